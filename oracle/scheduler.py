@@ -1,0 +1,280 @@
+"""Oracle FIFO scheduler (TEST INFRASTRUCTURE ONLY -- see ``oracle/__init__``).
+
+Follows:
+
+* *Continuous batching architecture* (HF Transformers docs), "Request
+  lifecycle": PENDING -> PREFILLING -> DECODING -> FINISHED, one output token
+  per decode step.
+* same page, "Chunked prefill": a prompt larger than the remaining token
+  budget (``max_batch_tokens``) is processed as far as the budget allows and
+  resumed next step from where it stopped.
+* same page, "Scheduler": token budget, cache budget (free KV pages) and the
+  request cap ``max_requests_per_batch``.
+* same page, "FIFO": active decodes first, then active prefills, then new
+  waiting requests in arrival order.
+* same page, "Admission": a request joins only if every allocator has room;
+  otherwise nothing is allocated.  ``safety_margin`` (FIFO default 0.15)
+  holds new prefills back when free capacity would fall below the margin.
+* same page, "Offloading": active requests that fail to get the blocks they
+  need are reported as stalled, with their block demand.
+* *vLLM serving internals*, "PagedAttention as a virtual memory system":
+  fixed 16-token blocks, a per-sequence block table from logical to physical
+  block, one more block when a sequence outgrows its last one, blocks back to
+  the pool when the sequence finishes; "What the scheduler looks like":
+  release finished, admit waiting while blocks allow, one batch per
+  iteration.
+* *Chunked Prefill* (Ultralytics glossary), "How chunked prefill works": one
+  token per running decode first, then chunks of waiting prompts fill the
+  remaining budget.
+
+Readings where the pages leave a step open:
+
+1. Batch order = decodes (admission order), active prefills (admission
+   order), newly admitted prompts (arrival order).
+2. Admission of waiting requests is strict head-of-line: the first waiting
+   request that does not fit (budget, request cap, blocks or margin) stops
+   admission for this step.
+3. A prefill chunk takes min(remaining prompt, remaining budget,
+   max_prefill_chunk) tokens (max_prefill_chunk = 0 means no cap).
+4. Blocks are allocated only for the tokens scheduled this step, all or
+   nothing per request.  The free list is a FIFO queue: allocation pops from
+   its head, freed blocks are pushed to its tail (finished requests in batch
+   order, each block table in logical order).
+5. The safety margin applies to admitting new requests only:
+   admit iff free_after >= ceil(margin * num_blocks), margin taken as an
+   IEEE float32 and the product computed in double precision.
+6. Decodes or prefills past the token budget or the request cap simply wait;
+   an active request whose blocks cannot be allocated is "stalled" and
+   reported with its demand.  A step that schedules nothing while requests
+   are stalled or waiting returns status NO_BLOCKS.
+7. The step that completes a prompt yields output token 1; each decode step
+   yields one more; a request with output_len n finishes after n-1 decode
+   steps.  A decode step's query token sits at position num_cached and its
+   K/V is appended in the same step.
+8. slot = block_table[pos // block_size] * block_size + pos % block_size.
+
+Parity: pinned by hand-derived traces (tests/golden/scheduler_*.json) and by
+invariants (budget, cap, FIFO order, block conservation, all-or-nothing
+admission); the full batch composition beyond the pages' rules rests on the
+readings above ("parity unpinned" beyond those pins).
+"""
+from __future__ import annotations
+
+import collections
+import math
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+
+WAITING, PREFILLING, DECODING, FINISHED = "waiting", "prefilling", "decoding", "finished"
+
+STATUS_OK = 0
+STATUS_NO_BLOCKS = 2
+
+
+class Request:
+    def __init__(self, req_id: int, prompt_len: int, output_len: int):
+        self.req_id = int(req_id)
+        self.prompt_len = int(prompt_len)
+        self.output_len = int(output_len)
+        self.num_cached = 0       # tokens whose K/V is in the cache
+        self.num_generated = 0    # output tokens produced so far
+        self.blocks: List[int] = []
+        self.state = WAITING
+
+
+class FifoScheduler:
+    def __init__(self, *, block_size: int, num_blocks: int,
+                 max_batch_tokens: int, max_requests_per_batch: int,
+                 max_blocks_per_seq: int, max_prefill_chunk: int = 0,
+                 safety_margin: float = 0.15,
+                 free_list: Optional[Sequence[int]] = None):
+        self.block_size = int(block_size)
+        self.num_blocks = int(num_blocks)
+        self.max_batch_tokens = int(max_batch_tokens)
+        self.max_requests_per_batch = int(max_requests_per_batch)
+        self.max_blocks_per_seq = int(max_blocks_per_seq)
+        self.max_prefill_chunk = int(max_prefill_chunk)
+        margin32 = float(np.float32(safety_margin))
+        self.reserved_blocks = int(math.ceil(margin32 * float(self.num_blocks)))
+        if free_list is None:
+            free_list = range(self.num_blocks)
+        self.free = collections.deque(int(b) for b in free_list)
+        self.waiting: collections.deque = collections.deque()
+        self.running: List[Request] = []
+        self.requests: Dict[int, Request] = {}
+        self._pending = None      # list of (request, num_tokens) of the open step
+
+    # ------------------------------------------------------------ requests
+    def _blocks_for(self, num_tokens: int) -> int:
+        return -(-num_tokens // self.block_size)
+
+    def add_request(self, req_id: int, prompt_len: int, output_len: int) -> None:
+        if req_id in self.requests or prompt_len < 1 or output_len < 1:
+            raise ValueError("bad request")
+        if self._blocks_for(prompt_len + output_len - 1) > self.max_blocks_per_seq:
+            raise ValueError("request longer than max_blocks_per_seq blocks")
+        r = Request(req_id, prompt_len, output_len)
+        self.requests[r.req_id] = r
+        self.waiting.append(r)
+
+    def add_running_request(self, req_id: int, prompt_len: int,
+                            output_len: int, num_cached: int) -> None:
+        """Resume a request whose first ``num_cached`` tokens already have K/V
+        in the cache (the swap-in path of "Offloading"): it joins the running
+        set after the requests already there, with ceil(num_cached/bs) blocks
+        taken from the free list."""
+        if req_id in self.requests or prompt_len < 1 or output_len < 1:
+            raise ValueError("bad request")
+        if num_cached < 0 or num_cached > prompt_len + output_len - 2:
+            raise ValueError("bad num_cached")
+        if self._blocks_for(prompt_len + output_len - 1) > self.max_blocks_per_seq:
+            raise ValueError("request longer than max_blocks_per_seq blocks")
+        need = self._blocks_for(num_cached)
+        if need > len(self.free):
+            raise MemoryError("not enough free blocks")
+        r = Request(req_id, prompt_len, output_len)
+        r.num_cached = num_cached
+        if num_cached >= prompt_len:
+            r.state = DECODING
+            r.num_generated = num_cached - prompt_len + 1
+        else:
+            r.state = PREFILLING
+        for _ in range(need):
+            r.blocks.append(self.free.popleft())
+        self.requests[r.req_id] = r
+        self.running.append(r)
+
+    def slots(self, req_id: int, start: int, count: int) -> np.ndarray:
+        r = self.requests[req_id]
+        out = np.empty(count, dtype=np.int32)
+        for i in range(count):
+            pos = start + i
+            out[i] = r.blocks[pos // self.block_size] * self.block_size + pos % self.block_size
+        return out
+
+    # ---------------------------------------------------------------- step
+    def schedule_step(self) -> dict:
+        if self._pending is not None:
+            raise RuntimeError("schedule_step called twice without step_done")
+        budget = self.max_batch_tokens
+        cap = self.max_requests_per_batch
+        batch = []            # (request, num_tokens)
+        stalled = []          # (req_id, blocks demanded)
+
+        # 1) active decodes, one token each, in admission order
+        for r in self.running:
+            if r.state != DECODING:
+                continue
+            if budget == 0 or len(batch) == cap:
+                break
+            need = self._blocks_for(r.num_cached + 1) - len(r.blocks)
+            if need > len(self.free):
+                stalled.append((r.req_id, need))
+                continue
+            for _ in range(need):
+                r.blocks.append(self.free.popleft())
+            batch.append((r, 1))
+            budget -= 1
+        num_decodes = len(batch)
+
+        # 2) active prefills, next chunk each, in admission order
+        for r in self.running:
+            if r.state != PREFILLING:
+                continue
+            if budget == 0 or len(batch) == cap:
+                break
+            n = min(r.prompt_len - r.num_cached, budget)
+            if self.max_prefill_chunk > 0:
+                n = min(n, self.max_prefill_chunk)
+            need = self._blocks_for(r.num_cached + n) - len(r.blocks)
+            if need > len(self.free):
+                stalled.append((r.req_id, need))
+                continue
+            for _ in range(need):
+                r.blocks.append(self.free.popleft())
+            batch.append((r, n))
+            budget -= n
+
+        # 3) waiting requests in arrival order, strict head-of-line
+        while self.waiting and budget > 0 and len(batch) < cap:
+            r = self.waiting[0]
+            n = min(r.prompt_len, budget)
+            if self.max_prefill_chunk > 0:
+                n = min(n, self.max_prefill_chunk)
+            need = self._blocks_for(n)
+            if len(self.free) - need < self.reserved_blocks:
+                break
+            self.waiting.popleft()
+            for _ in range(need):
+                r.blocks.append(self.free.popleft())
+            r.state = PREFILLING
+            self.running.append(r)
+            batch.append((r, n))
+            budget -= n
+
+        status = STATUS_OK
+        if not batch and (stalled or self.waiting):
+            status = STATUS_NO_BLOCKS
+        step = self._emit(batch, num_decodes, stalled, status)
+        # an OK step (possibly empty) is committed by step_done; a NO_BLOCKS
+        # step allocated nothing and leaves nothing to commit
+        self._pending = batch if status == STATUS_OK else None
+        return step
+
+    def _emit(self, batch, num_decodes, stalled, status) -> dict:
+        R = len(batch)
+        cu = np.zeros(R + 1, dtype=np.int32)
+        seq_lens = np.zeros(R, dtype=np.int32)
+        tables = np.full((R, self.max_blocks_per_seq), -1, dtype=np.int32)
+        req_ids = np.zeros(R, dtype=np.int64)
+        slots = []
+        for i, (r, n) in enumerate(batch):
+            req_ids[i] = r.req_id
+            cu[i + 1] = cu[i] + n
+            seq_lens[i] = r.num_cached + n
+            tables[i, :len(r.blocks)] = r.blocks
+            for pos in range(r.num_cached, r.num_cached + n):
+                slots.append(r.blocks[pos // self.block_size] * self.block_size
+                             + pos % self.block_size)
+        return {
+            "status": status,
+            "num_reqs": R,
+            "num_tokens": int(cu[-1]),
+            "num_decodes": num_decodes,
+            "req_ids": req_ids,
+            "cu_seqlens_q": cu,
+            "seq_lens": seq_lens,
+            "block_tables": tables,
+            "slot_mapping": np.asarray(slots, dtype=np.int32),
+            "stalled_ids": np.asarray([s[0] for s in stalled], dtype=np.int64),
+            "stalled_demand": np.asarray([s[1] for s in stalled], dtype=np.int32),
+        }
+
+    def step_done(self) -> List[int]:
+        """Commit the open step; returns the ids of requests that finished."""
+        if self._pending is None:
+            raise RuntimeError("no open step")
+        finished = []
+        for r, n in self._pending:
+            r.num_cached += n
+            if r.state == PREFILLING:
+                if r.num_cached == r.prompt_len:
+                    r.num_generated = 1
+                    r.state = DECODING
+            else:
+                r.num_generated += 1
+            if r.state == DECODING and r.num_generated >= r.output_len:
+                r.state = FINISHED
+                finished.append(r)
+        for r in finished:
+            self.running.remove(r)
+            for b in r.blocks:
+                self.free.append(b)
+            r.blocks = []
+        self._pending = None
+        return [r.req_id for r in finished]
+
+    # -------------------------------------------------------------- counts
+    def counts(self):
+        return len(self.free), len(self.waiting), len(self.running)

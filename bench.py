@@ -1,0 +1,543 @@
+#!/usr/bin/env python3
+"""Benchmark: attention tokens/s of one continuous-batching step.
+
+Workload (default ``mixed_2048``): the mixed chunked-prefill step -- 96 decode
+requests (contexts U[256, 8192]), one prefill in flight on its second 1024-
+token chunk (prompt 3000), new prompts U[64, 1024] filling a 2048-token
+budget; 32 query / 8 KV heads, head_dim 128, bf16, 16-token blocks, a 65,536-
+block pool with permuted physical blocks.  One step = cb_kv_append of the
+step's new K/V + cb_paged_attention over the whole mixed batch.
+
+JSON line keys (rank 0):
+  value        tokens of the step / time of append+attention, inputs resident
+               in HBM (KV read per step 1.7 GB >> 129 MB L2, so no flush).
+  e2e          the same step through the public API with host buffers: C
+               scheduler call, metadata + q/k/v host->device from pinned
+               memory, append + attention, output device->host.
+  roofline     the dominant kernel (split-KV decode): algorithmic bytes per
+               launch / its CUDA-event duration, against measured HBM peak.
+  prefill      the prefill-chunk kernel: algorithmic FLOPs / duration.
+  cpu_baseline the CPU oracle on a bounded sample of the same step.
+
+``--impl reference`` times the CPU oracle instead (bounded sample per step).
+Multi-GPU: one process per GPU (torchrun), each an independent replica of
+the workload (requests shard across GPUs with no exchange): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the decode
+# kernel on this workload (profiles/decode_mixed_2048.md); None until taken
+# for the current kernel.
+DECODE_TRAFFIC_BYTES = None
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- work models
+def decode_bytes(step, Hq, Hkv, D, elem):
+    """Algorithmic bytes of the decode rows: each cached K and V row read once
+    per KV head, plus q read and out written."""
+    nd = step["num_decodes"]
+    seq = np.asarray(step["seq_lens"][:nd], dtype=np.int64)
+    return int(seq.sum() * Hkv * D * 2 * elem + nd * Hq * D * 2 * elem)
+
+
+def prefill_flops(step, Hq, D):
+    """Algorithmic FLOPs of the prefill rows: 2*D for q.k and 2*D for p.v per
+    unmasked (query, key) pair and query head."""
+    nd = step["num_decodes"]
+    cu = np.asarray(step["cu_seqlens_q"], dtype=np.int64)
+    seq = np.asarray(step["seq_lens"], dtype=np.int64)
+    pairs = 0
+    for r in range(nd, step["num_reqs"]):
+        n = int(cu[r + 1] - cu[r])
+        start = int(seq[r]) - n
+        pairs += n * start + n * (n + 1) // 2
+    return int(4 * D * Hq * pairs)
+
+
+def append_bytes(step, Hkv, D, elem):
+    return int(step["num_tokens"] * Hkv * D * 2 * elem * 2)
+
+
+# ---------------------------------------------------------- the workload
+def build_scenario(name):
+    return workloads.SCENARIOS[name]()
+
+
+def load_c_scheduler(cb, sc):
+    s = cb.Scheduler(block_size=sc.block_size, num_blocks=sc.num_blocks,
+                     max_batch_tokens=sc.max_batch_tokens,
+                     max_requests_per_batch=sc.max_requests_per_batch,
+                     max_blocks_per_seq=sc.max_blocks_per_seq,
+                     max_prefill_chunk=sc.max_prefill_chunk, safety_margin=sc.safety_margin,
+                     free_list=sc.free_list)
+    for r in sc.running:
+        s.add_running_request(r.req_id, r.prompt_len, r.output_len, r.num_cached)
+    for w in sc.waiting:
+        s.add_request(w.req_id, w.prompt_len, w.output_len)
+    return s
+
+
+def _sub_step(step, lo, hi):
+    """Host metadata of rows [lo, hi) as a stand-alone step."""
+    cu = np.asarray(step["cu_seqlens_q"])
+    sub = dict(step)
+    sub["num_reqs"] = hi - lo
+    sub["cu_seqlens_q"] = (cu[lo:hi + 1] - cu[lo]).astype(np.int32)
+    sub["seq_lens"] = np.asarray(step["seq_lens"])[lo:hi]
+    sub["block_tables"] = np.asarray(step["block_tables"])[lo:hi]
+    sub["slot_mapping"] = np.asarray(step["slot_mapping"])[cu[lo]:cu[hi]]
+    sub["num_tokens"] = int(cu[hi] - cu[lo])
+    sub["num_decodes"] = max(0, min(step["num_decodes"], hi) - lo)
+    sub["max_q_len"] = int(np.diff(sub["cu_seqlens_q"]).max(initial=1))
+    sub["max_seq_len"] = int(np.max(sub["seq_lens"], initial=1))
+    return sub
+
+
+def time_loop(torch, fn, iters, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(iters):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3  # seconds
+
+
+# ----------------------------------------------------------- CPU oracle
+def oracle_sample(sc, step, pools_cpu, rows, prefill_token_cap=None):
+    """Run the oracle on ``rows`` of ``step``: gather each row's cache blocks
+    into its own float64 sub-pool, append the row's new K/V, attend (for a
+    prefill row, optionally only its last ``prefill_token_cap`` queries).
+    Returns (query tokens processed, seconds)."""
+    from oracle import attention as oatt
+    from oracle import paged_kv
+    kp, vp, kn, vn, q = pools_cpu
+    bs = sc.block_size
+    cu = step["cu_seqlens_q"]
+    t0 = time.perf_counter()
+    ntok = 0
+    for r in rows:
+        a, b = int(cu[r]), int(cu[r + 1])
+        L = int(step["seq_lens"][r])
+        a2 = b - prefill_token_cap if (prefill_token_cap and b - a > prefill_token_cap) else a
+        blocks = [int(x) for x in step["block_tables"][r] if x >= 0]
+        sub_k = kp[blocks].astype(np.float64)
+        sub_v = vp[blocks].astype(np.float64)
+        table = np.arange(len(blocks))
+        local = {blk: i for i, blk in enumerate(blocks)}
+        slots = [local[int(s) // bs] * bs + int(s) % bs for s in step["slot_mapping"][a:b]]
+        paged_kv.append(sub_k, sub_v, kn[a:b].astype(np.float64), vn[a:b].astype(np.float64),
+                        np.asarray(slots), bs)
+        K = oatt.gather_kv(sub_k, table, L, bs)
+        V = oatt.gather_kv(sub_v, table, L, bs)
+        oatt.attend_one_request(q[a2:b].astype(np.float64), K, V, L - (b - a2), sc.softmax_scale)
+        ntok += b - a2
+    return ntok, time.perf_counter() - t0
+
+
+def choose_oracle_rows(step, budget_rows):
+    nd = step["num_decodes"]
+    R = step["num_reqs"]
+    dec = list(np.linspace(0, nd - 1, num=min(nd, budget_rows), dtype=int)) if nd else []
+    pre = list(range(nd, R))
+    return sorted(set(int(x) for x in dec)), pre
+
+
+# ----------------------------------------------------------------- main
+def run_ours(args, rank, world):
+    import torch
+    import paged_attention_continuous_gb300 as cb
+    from paged_attention_continuous_gb300.step import StepRunner
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    sc = build_scenario(args.workload)
+    elem = 2 if sc.dtype == "bf16" else 4
+    sched = load_c_scheduler(cb, sc)
+    step = sched.schedule_step()
+    assert step["status"] == 0
+    T, R, nd = step["num_tokens"], step["num_reqs"], step["num_decodes"]
+    runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
+                        num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim, dtype=sc.dtype,
+                        max_reqs=sc.max_requests_per_batch, max_tokens=sc.max_batch_tokens,
+                        max_blocks_per_seq=sc.max_blocks_per_seq, zero_cache=False)
+    # initial pool contents stand for K/V written by earlier steps
+    runner.k_cache[0].copy_(workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size,
+                                                 sc.head_dim, seed=1234, dtype=sc.dtype,
+                                                 scale=sc.value_scale, device=dev))
+    runner.v_cache[0].copy_(workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size,
+                                                 sc.head_dim, seed=1235, dtype=sc.dtype,
+                                                 scale=sc.value_scale, device=dev))
+    seeds = [workloads.step_seed(sc.seed, 0, 0, w) for w in range(3)]
+    q = workloads.token_tensors(T, sc.num_q_heads, sc.head_dim, seed=seeds[0], dtype=sc.dtype,
+                                scale=sc.value_scale, device=dev)
+    k = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[1], dtype=sc.dtype,
+                                scale=sc.value_scale, device=dev)
+    v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[2], dtype=sc.dtype,
+                                scale=sc.value_scale, device=dev)
+    out = torch.empty_like(q)
+    ds = runner.upload(step)
+    stream = torch.cuda.current_stream()
+    ws = runner.workspace
+    kc, vc = runner.k_cache[0], runner.v_cache[0]
+
+    def full_step():
+        runner.run(ds, q, k, v, out=out)
+
+    # decode-only and prefill-only views for per-kernel timing
+    dstep = _sub_step(step, 0, nd)
+    pstep = _sub_step(step, nd, R)
+
+    def make_attn(sub, tok_lo):
+        import torch as _t
+        if sub["num_reqs"] == 0:
+            return None
+        cu = _t.from_numpy(np.asarray(sub["cu_seqlens_q"], dtype=np.int32)).to(dev)
+        sl = _t.from_numpy(np.asarray(sub["seq_lens"], dtype=np.int32)).to(dev)
+        bt = _t.from_numpy(np.ascontiguousarray(sub["block_tables"], dtype=np.int32)).to(dev)
+        qs = q[tok_lo:tok_lo + sub["num_tokens"]]
+        os_ = out[tok_lo:tok_lo + sub["num_tokens"]]
+
+        def f():
+            cb.paged_attention(qs, kc, vc, cu, sl, bt, num_decodes=sub["num_decodes"],
+                               max_q_len=sub["max_q_len"], max_seq_len=sub["max_seq_len"],
+                               scale=sc.softmax_scale, workspace=ws, out=os_)
+        return f
+
+    dec_fn = make_attn(dstep, 0)
+    pre_fn = make_attn(pstep, nd)
+
+    W, K = args.warmup, args.steps
+    for _ in range(W):
+        full_step()
+        if dec_fn:
+            dec_fn()
+        if pre_fn:
+            pre_fn()
+    torch.cuda.synchronize()
+    assert ws.read_errors() == 0
+
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    t_step = time_loop(torch, full_step, K, stream)
+    t_dec = time_loop(torch, dec_fn, K, stream) if dec_fn else 0.0
+    t_pre = time_loop(torch, pre_fn, K, stream) if pre_fn else 0.0
+    clk = clocks.stop()
+    if world > 1:
+        tt = torch.tensor([t_step], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_step = float(tt.item())
+        torch.distributed.barrier()
+    assert ws.read_errors() == 0
+
+    # ---- end to end through the public API, host buffers
+    e2e_steps = min(K, args.e2e_steps)
+    scheds = [load_c_scheduler(cb, sc) for _ in range(e2e_steps + 1)]
+    hq = q.cpu().pin_memory(); hk = k.cpu().pin_memory(); hv = v.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step(s):
+        st = s.schedule_step()
+        d = runner.upload(st)
+        dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+        runner.run(d, dq, dk, dv, out=out)
+        hout.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return d.h2d_bytes
+
+    e2e_step(scheds[-1])  # warm
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    h2d_meta = 0
+    for i in range(e2e_steps):
+        h2d_meta = e2e_step(scheds[i])
+    t_e2e = time.perf_counter() - t0
+    h2d = h2d_meta + (hq.numel() + hk.numel() + hv.numel()) * hq.element_size()
+    d2h = hout.numel() * hout.element_size()
+
+    pk, src = peaks()
+    hbm = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bf16 = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    bf16s = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    dbytes = decode_bytes(step, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, elem)
+    pflops = prefill_flops(step, sc.num_q_heads, sc.head_dim)
+    dec_s = t_dec / K if K else 0.0
+    pre_s = t_pre / K if K else 0.0
+    dec_gbs = dbytes / dec_s / 1e9 if dec_s else 0.0
+    pre_tflops = pflops / pre_s / 1e12 if pre_s else 0.0
+    step_s = t_step / K
+    dec_launches = (nd + 1023) // 1024
+    pre_launches = 1 if R > nd else 0
+    launches = K * (1 + dec_launches + pre_launches) + K * dec_launches + K * pre_launches
+
+    line = {
+        "metric": "attention tokens/s per mixed step",
+        "value": round(T * world / step_s, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(step_s * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": sc.dtype,
+        "data": "synthetic (seeded N(0,1)*0.5 q/k/v, random-filled KV pool, permuted blocks)",
+        "config": {"workload": sc.name, "num_tokens": T, "num_reqs": R, "num_decodes": nd,
+                   "q_heads": sc.num_q_heads, "kv_heads": sc.num_kv_heads,
+                   "head_dim": sc.head_dim, "block_size": sc.block_size,
+                   "num_blocks": sc.num_blocks, "max_batch_tokens": sc.max_batch_tokens,
+                   "l2": "inputs larger than L2 (decode KV %.2f GB per step), no flush" % (dbytes / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(T * e2e_steps * world / t_e2e, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "steps": e2e_steps,
+                "includes": "cb_schedule_step + pinned H2D of metadata and q/k/v + "
+                            "cb_kv_append + cb_paged_attention + D2H of output"},
+        "roofline": {"kernel": "decode_kernel (split-KV, bf16)", "bound": "hbm",
+                     "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(dec_gbs / hbm, 4), "peak_source": src,
+                     "traffic": DECODE_TRAFFIC_BYTES,
+                     "algorithmic_bytes_per_launch": dbytes,
+                     "ms_per_launch": round(dec_s * 1e3, 4)},
+        "prefill": {"kernel": "prefill rows", "bound": "tensor",
+                    "achieved": round(pre_tflops, 2), "peak": bf16, "unit": "TFLOP/s",
+                    "frac": round(pre_tflops / bf16, 4),
+                    "frac_sustained": round(pre_tflops / bf16s, 4), "peak_source": src,
+                    "algorithmic_flops_per_launch": pflops,
+                    "ms_per_launch": round(pre_s * 1e3, 4)},
+        "append": {"bytes_per_step": append_bytes(step, sc.num_kv_heads, sc.head_dim, elem)},
+        "clocks": clk,
+        "gpu_launches": int(launches),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sc, step, runner, q, k, v, torch, dev,
+                                            budget_s=args.cpu_seconds)
+    return line
+
+
+def _pristine_blocks(sc, blocks, dev, torch):
+    kp = workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size, sc.head_dim,
+                              seed=1234, dtype=sc.dtype, scale=sc.value_scale, device=dev)
+    vp = workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size, sc.head_dim,
+                              seed=1235, dtype=sc.dtype, scale=sc.value_scale, device=dev)
+    sel = torch.tensor(blocks, dtype=torch.long, device=dev)
+    k = kp.index_select(0, sel).float().cpu().numpy()
+    v = vp.index_select(0, sel).float().cpu().numpy()
+    del kp, vp
+    return k, v
+
+
+def cpu_baseline(sc, step, runner, q, k, v, torch, dev, budget_s=20.0, impl_line=False):
+    """The oracle, as it stands, on a bounded sample of the step: a spread of
+    decode rows plus the prefill rows (their last queries), timed on the host
+    cores."""
+    dec_rows, pre_rows = choose_oracle_rows(step, 16)
+    rows = dec_rows + pre_rows
+    blocks = sorted({int(b) for r in rows for b in step["block_tables"][r] if b >= 0})
+    kpool, vpool = _pristine_blocks(sc, blocks, dev, torch)
+    remap = {b: i for i, b in enumerate(blocks)}
+    st = dict(step)
+    bt = np.full_like(np.asarray(step["block_tables"]), -1)
+    for r in rows:
+        for c, b in enumerate(step["block_tables"][r]):
+            if b >= 0:
+                bt[r, c] = remap[int(b)]
+    st["block_tables"] = bt
+    st["slot_mapping"] = np.asarray([remap[int(s) // sc.block_size] * sc.block_size +
+                                     int(s) % sc.block_size if (int(s) // sc.block_size) in remap
+                                     else -1 for s in step["slot_mapping"]], dtype=np.int64)
+    pools = (kpool, vpool, k.float().cpu().numpy(), v.float().cpu().numpy(), q.float().cpu().numpy())
+    # size the prefill slice so one sample takes about budget_s
+    n, t = oracle_sample(sc, st, pools, dec_rows)
+    cap = 64
+    n2, t2 = oracle_sample(sc, st, pools, pre_rows, prefill_token_cap=cap)
+    per_tok = t2 / max(n2, 1)
+    room = max(budget_s - t, 0.5)
+    cap = int(max(16, min(2048, room / max(per_tok, 1e-6) / max(len(pre_rows), 1))))
+    n2, t2 = oracle_sample(sc, st, pools, pre_rows, prefill_token_cap=cap)
+    try:
+        import threadpoolctl
+        threads = max(p.get("num_threads", 1) for p in threadpoolctl.threadpool_info())
+    except Exception:
+        threads = os.cpu_count()
+    return {"value": round((n + n2) / (t + t2), 2), "unit": "tokens/s",
+            "cores": int(threads), "host_cpus": os.cpu_count(), "kind": "oracle",
+            "seconds": round(t + t2, 2),
+            "sample": f"{sc.name} step 0: {len(dec_rows)} of {step['num_decodes']} decode rows "
+                      f"+ the last {cap} queries of each of {len(pre_rows)} prefill rows "
+                      f"({n + n2} query tokens), numpy float64"}
+
+
+def run_reference(args, rank, world):
+    """CPU oracle on the same workload, a bounded sample per step."""
+    if rank != 0:
+        return None
+    import torch
+    sc = build_scenario(args.workload)
+    from oracle.scheduler import FifoScheduler
+    o = FifoScheduler(block_size=sc.block_size, num_blocks=sc.num_blocks,
+                      max_batch_tokens=sc.max_batch_tokens,
+                      max_requests_per_batch=sc.max_requests_per_batch,
+                      max_blocks_per_seq=sc.max_blocks_per_seq,
+                      max_prefill_chunk=sc.max_prefill_chunk, safety_margin=sc.safety_margin,
+                      free_list=sc.free_list)
+    for r in sc.running:
+        o.add_running_request(r.req_id, r.prompt_len, r.output_len, r.num_cached)
+    for w in sc.waiting:
+        o.add_request(w.req_id, w.prompt_len, w.output_len)
+    step = o.schedule_step()
+    step["max_q_len"] = int(np.diff(step["cu_seqlens_q"]).max())
+    step["max_seq_len"] = int(step["seq_lens"].max())
+    T = step["num_tokens"]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    seeds = [workloads.step_seed(sc.seed, 0, 0, w) for w in range(3)]
+    q = workloads.token_tensors(T, sc.num_q_heads, sc.head_dim, seed=seeds[0], dtype=sc.dtype,
+                                scale=sc.value_scale, device=dev)
+    k = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[1], dtype=sc.dtype,
+                                scale=sc.value_scale, device=dev)
+    v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[2], dtype=sc.dtype,
+                                scale=sc.value_scale, device=dev)
+    total = args.steps + args.warmup
+    budget = max(0.2, min(20.0, 150.0 / max(total, 1)))
+    tot_tok, tot_s = 0, 0.0
+    for i in range(total):
+        cb = cpu_baseline(sc, step, None, q, k, v, torch, dev, budget_s=budget)
+        if i >= args.warmup:
+            tot_tok += cb["value"] * cb["seconds"]
+            tot_s += cb["seconds"]
+    val = tot_tok / tot_s if tot_s else 0.0
+    return {"impl": "reference", "metric": "attention tokens/s per mixed step",
+            "value": round(val, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(tot_s / max(args.steps, 1) * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": sc.name},
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"],
+                             "value": round(val, 2)},
+            "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixed_2048",
+                    choices=["mixed_2048", "decode_64", "long_prompt_32k"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

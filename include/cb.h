@@ -1,0 +1,273 @@
+/*
+ * cb.h -- C ABI of the GB300 continuous-batching paged-attention step.
+ *
+ * One serving step of a continuous-batching engine with chunked prefill and
+ * a paged KV cache:
+ *
+ *   1. cb_schedule_step  (host)  picks the batch: one token per running
+ *      decode, then prefill chunks, under a token budget, a request cap and
+ *      the free-block budget, and emits the step's metadata
+ *      (cu_seqlens_q, seq_lens, block_tables, slot_mapping).
+ *   2. cb_kv_append      (GPU)   writes the step's new K/V into the paged
+ *      cache at slot_mapping.
+ *   3. cb_paged_attention(GPU)   every scheduled query attends, causally over
+ *      absolute positions, to its request's K/V read through its block table.
+ *   4. cb_step_done      (host)  commits the step: advances each request,
+ *      finishes requests and returns their blocks to the pool.
+ *
+ * Sources (page title, section):
+ *   - "Continuous batching architecture" (HF Transformers docs): Request
+ *     lifecycle; Chunked prefill; Scheduler (token budget max_batch_tokens,
+ *     cache budget, request cap max_requests_per_batch); FIFO; Admission
+ *     (all-or-nothing, safety_margin); Offloading (stalled requests and their
+ *     block demand).
+ *   - "Chunked Prefill" (Ultralytics glossary): How chunked prefill works
+ *     (decode tokens first, then chunks; each chunk attends under a causal
+ *     mask over absolute positions to all earlier chunks plus itself).
+ *   - "vLLM serving internals" (AI Engineering from Scratch, phase 17 lesson
+ *     04): PagedAttention as a virtual memory system (fixed 16-token blocks,
+ *     per-sequence block tables, blocks back to the pool on finish);
+ *     Iteration-level continuous batching; What the scheduler looks like.
+ *
+ * Conventions for every call:
+ *   - Every function returns cb_status; CB_OK == 0.  On failure
+ *     cb_last_error() returns a thread-local message.  No C++ exception
+ *     crosses this boundary.
+ *   - GPU calls are asynchronous on the given stream (a cudaStream_t passed
+ *     as cb_stream_t; NULL = legacy default stream).  Argument errors are
+ *     detected on the host before anything is launched.  Errors found on
+ *     the device (a block id outside the pool, a slot outside the cache, a
+ *     decode row whose query length is not 1, a timed-out wait) set bits in
+ *     the workspace's device error word instead of faulting; read them with
+ *     cb_attention_read_errors.
+ *   - All device pointers are caller-owned (e.g. allocated by PyTorch) and
+ *     must stay valid until the stream has executed the call.  Nothing here
+ *     allocates device memory; the attention workspace is sized by
+ *     cb_attention_workspace_size and owned by the caller.
+ *   - Cache layout: k_cache and v_cache are [num_blocks][Hkv][block_size][D],
+ *     row-major, so one (block, KV head) page of block_size x D elements is
+ *     contiguous.  Token tensors are [tokens][heads][D].  block_size is 16.
+ */
+#ifndef CB_H_
+#define CB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cb_stream_t; /* same type as cudaStream_t */
+
+typedef enum cb_status {
+  CB_OK = 0,
+  CB_ERR_INVALID_ARG = 1,   /* bad argument; nothing was changed or launched */
+  CB_ERR_NO_BLOCKS = 2,     /* no batch could be scheduled: the cache is full
+                               (see cb_step.stalled_*) or the next waiting
+                               request does not fit */
+  CB_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+  CB_ERR_UNSUPPORTED = 4,   /* valid but not implemented shape/dtype */
+  CB_ERR_DEVICE_CHECK = 5,  /* a kernel reported bad metadata (see
+                               cb_attention_read_errors) */
+  CB_ERR_STATE = 6          /* call out of order (e.g. two schedule calls
+                               without cb_step_done) */
+} cb_status;
+
+typedef enum cb_dtype {
+  CB_DTYPE_F32 = 0,         /* float32 storage, float32 arithmetic */
+  CB_DTYPE_BF16 = 1         /* bfloat16 storage, float32 accumulation,
+                               outputs rounded to nearest even */
+} cb_dtype;
+
+/* Returns the message of the last failed call on this thread ("" if none). */
+const char* cb_last_error(void);
+
+/* ABI version, (major << 16) | minor. */
+int32_t cb_version(void);
+
+/* ------------------------------------------------------------------------
+ * Scheduler (host).
+ * "Continuous batching architecture", sections Scheduler / FIFO / Admission /
+ * Offloading; "vLLM serving internals", What the scheduler looks like.
+ * ---------------------------------------------------------------------- */
+typedef struct cb_config {
+  int32_t block_size;             /* tokens per KV block; > 0 */
+  int32_t num_blocks;             /* blocks in the pool; > 0 */
+  int32_t max_batch_tokens;       /* token budget per step; > 0 */
+  int32_t max_requests_per_batch; /* request cap per step (decodes count); > 0 */
+  int32_t max_prefill_chunk;      /* per-request prefill chunk cap; 0 = none */
+  int32_t max_blocks_per_seq;     /* width of a block_tables row; a request
+                                     whose prompt_len+output_len-1 tokens need
+                                     more blocks is rejected */
+  float safety_margin;            /* fraction of num_blocks that must stay
+                                     free after admitting a NEW request:
+                                     admit iff free_after >=
+                                     ceil((double)margin * num_blocks).
+                                     FIFO default 0.15; 0 disables it */
+  const int32_t* initial_free_list; /* optional host array of num_blocks
+                                       distinct ids in [0, num_blocks): the
+                                       allocation order; NULL = 0,1,2,...
+                                       Copied; not retained. */
+} cb_config;
+
+typedef struct cb_sched cb_sched;
+
+/* One scheduled step.  All arrays are HOST memory owned by the scheduler,
+ * valid until the next cb_schedule_step or cb_sched_destroy.  Batch order:
+ * decodes (admission order), then running prefills (admission order), then
+ * newly admitted prompts (arrival order). */
+typedef struct cb_step {
+  int32_t num_reqs;              /* R */
+  int32_t num_tokens;            /* T = cu_seqlens_q[R] */
+  int32_t num_decodes;           /* the first num_decodes rows are decodes
+                                    (exactly one query token each) */
+  int32_t max_q_len;             /* max over rows of the query length */
+  int32_t max_seq_len;           /* max over rows of seq_lens */
+  int32_t max_blocks_per_seq;    /* row stride of block_tables */
+  const int64_t* req_ids;        /* [R] */
+  const int32_t* cu_seqlens_q;   /* [R+1] prefix sums of query lengths */
+  const int32_t* seq_lens;       /* [R] tokens in the cache after this step's
+                                    append (cached + scheduled) */
+  const int32_t* block_tables;   /* [R][max_blocks_per_seq], -1 padded */
+  const int32_t* slot_mapping;   /* [T] block*block_size + offset of each new
+                                    token's K/V */
+  int32_t num_stalled;           /* active requests that could not get the
+                                    blocks they need this step */
+  const int64_t* stalled_ids;    /* [num_stalled] */
+  const int32_t* stalled_demand; /* [num_stalled] blocks each one needs */
+} cb_step;
+
+/* Create / destroy a scheduler.  *out is NULL on failure. */
+cb_status cb_sched_create(const cb_config* cfg, cb_sched** out);
+void cb_sched_destroy(cb_sched* s);
+
+/* Queue a new request (state PENDING); arrival order = call order.
+ * CB_ERR_INVALID_ARG for a duplicate id, prompt_len < 1, output_len < 1 or a
+ * request longer than max_blocks_per_seq blocks. */
+cb_status cb_add_request(cb_sched* s, int64_t req_id, int32_t prompt_len,
+                         int32_t output_len);
+
+/* Resume a request whose first num_cached tokens already have K/V in the
+ * cache (the swap-in path of "Offloading": resume without recomputing).  It
+ * joins the running set after the requests already there and takes
+ * ceil(num_cached / block_size) blocks from the free list.  If num_cached >=
+ * prompt_len it is DECODING with num_cached - prompt_len + 1 tokens generated
+ * (requires num_cached <= prompt_len + output_len - 2), else PREFILLING.
+ * CB_ERR_NO_BLOCKS if the pool is too small (nothing allocated). */
+cb_status cb_add_running_request(cb_sched* s, int64_t req_id,
+                                 int32_t prompt_len, int32_t output_len,
+                                 int32_t num_cached);
+
+/* Schedule the next step (FIFO policy).  Returns CB_OK with a possibly empty
+ * batch, or CB_ERR_NO_BLOCKS when nothing could be scheduled although
+ * requests are stalled or waiting; *out is filled in both cases.  After
+ * CB_OK the caller runs the step and then must call cb_step_done before the
+ * next cb_schedule_step (CB_ERR_STATE otherwise). */
+cb_status cb_schedule_step(cb_sched* s, cb_step* out);
+
+/* Commit the last CB_OK step.  *num_finished / *finished_ids (host, owned by
+ * the scheduler, valid until the next call) list requests that finished, in
+ * batch order; their blocks went back to the tail of the free list.  Either
+ * output pointer may be NULL. */
+cb_status cb_step_done(cb_sched* s, int32_t* num_finished,
+                       const int64_t** finished_ids);
+
+/* slots_out[i] = slot of position start+i of request req_id (positions must
+ * lie inside the request's allocated blocks). */
+cb_status cb_request_slots(const cb_sched* s, int64_t req_id, int32_t start,
+                           int32_t count, int32_t* slots_out);
+
+/* Pool and queue sizes; any output pointer may be NULL. */
+cb_status cb_sched_counts(const cb_sched* s, int32_t* free_blocks,
+                          int32_t* num_waiting, int32_t* num_running);
+
+/* Copies the free list (allocation order) into out[0..capacity); *count gets
+ * its length. */
+cb_status cb_sched_free_list(const cb_sched* s, int32_t* out, int32_t capacity,
+                             int32_t* count);
+
+/* ------------------------------------------------------------------------
+ * cb_kv_append (GPU).  "vLLM serving internals", PagedAttention as a virtual
+ * memory system: token t's K/V goes to block slot_mapping[t] / block_size,
+ * offset slot_mapping[t] % block_size, for every KV head.
+ *
+ *   k_new, v_new  device [num_tokens][Hkv][D] (dtype)
+ *   slot_mapping  device int32 [num_tokens]; -1 = padding, skipped
+ *   k_cache, v_cache device [num_blocks][Hkv][block_size][D] (dtype)
+ *   error_word    optional device uint32; a slot >= num_blocks*block_size is
+ *                 skipped and sets CB_DEVERR_SLOT_RANGE there.
+ * D * sizeof(dtype) must be a multiple of 16 bytes and every pointer 16-byte
+ * aligned.  Bit-exact copy.
+ * ---------------------------------------------------------------------- */
+cb_status cb_kv_append(const void* k_new, const void* v_new,
+                       const int32_t* slot_mapping, int32_t num_tokens,
+                       void* k_cache, void* v_cache, int32_t num_blocks,
+                       int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, cb_dtype dtype,
+                       uint32_t* error_word, cb_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * cb_paged_attention (GPU).  "Chunked Prefill", How chunked prefill works:
+ * query i of row r (absolute position p = seq_lens[r] - q_len + i) attends
+ * to keys 0..p of its own request, read through block_tables[r]:
+ *   out[t,h] = sum_{j<=p} softmax_j(scale * q[t,h].k[j,g]) v[j,g],
+ *   g = h / (Hq/Hkv).
+ * Rows [0, num_decodes) must have query length 1 and run the split-KV decode
+ * kernel; the remaining rows run the prefill-chunk kernel.
+ * ---------------------------------------------------------------------- */
+typedef struct cb_attention_args {
+  const void* q;                /* device [num_tokens][Hq][D] */
+  void* out;                    /* device [num_tokens][Hq][D], same dtype */
+  const void* k_cache;          /* device [num_blocks][Hkv][block_size][D] */
+  const void* v_cache;          /* same layout */
+  const int32_t* cu_seqlens_q;  /* device [num_reqs+1] */
+  const int32_t* seq_lens;      /* device [num_reqs] */
+  const int32_t* block_tables;  /* device [num_reqs][max_blocks_per_seq] */
+  int32_t num_reqs;
+  int32_t num_decodes;          /* rows [0, num_decodes) are decodes */
+  int32_t num_tokens;
+  int32_t max_q_len;            /* host bound on rows' query length */
+  int32_t max_seq_len;          /* host bound on seq_lens */
+  int32_t num_blocks;           /* pool size (block ids are range-checked) */
+  int32_t max_blocks_per_seq;
+  int32_t block_size;           /* must be 16 */
+  int32_t num_q_heads;          /* Hq, a multiple of Hkv */
+  int32_t num_kv_heads;         /* Hkv */
+  int32_t head_dim;             /* D: 64 or 128 */
+  float scale;                  /* softmax scale, usually 1/sqrt(D) */
+  cb_dtype dtype;
+  void* workspace;              /* device, >= cb_attention_workspace_size(),
+                                   256-byte aligned, zeroed once by
+                                   cb_attention_workspace_init; calls leave it
+                                   ready for the next call */
+  size_t workspace_bytes;
+} cb_attention_args;
+
+/* Device error bits (cb_attention_read_errors / cb_kv_append error_word). */
+#define CB_DEVERR_BLOCK_RANGE 0x1u  /* block id outside [0, num_blocks) */
+#define CB_DEVERR_SLOT_RANGE 0x2u   /* slot outside the cache */
+#define CB_DEVERR_DECODE_QLEN 0x4u  /* a decode row with query length != 1 */
+#define CB_DEVERR_SEQ_RANGE 0x8u    /* seq_len < q_len or beyond the table */
+#define CB_DEVERR_TIMEOUT 0x10u     /* a bounded wait ran out */
+
+/* Workspace bytes for a call with these sizes (upper bound; 0 on bad args). */
+size_t cb_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim);
+
+/* Zero a freshly allocated workspace (async on stream).  Needed once; after
+ * a CB_ERR_DEVICE_CHECK, call it again. */
+cb_status cb_attention_workspace_init(void* workspace, size_t workspace_bytes,
+                                      cb_stream_t stream);
+
+cb_status cb_paged_attention(const cb_attention_args* args, cb_stream_t stream);
+
+/* Synchronizes the stream and reads (and clears) the device error word of a
+ * workspace.  Returns CB_ERR_DEVICE_CHECK if any bit was set. */
+cb_status cb_attention_read_errors(void* workspace, size_t workspace_bytes,
+                                   cb_stream_t stream, uint32_t* bits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CB_H_ */

@@ -1,0 +1,325 @@
+"""GB300 continuous-batching paged attention: Python binding of ``libcb.so``.
+
+A thin ctypes layer over the C ABI declared in ``include/cb.h``; it only
+marshals arguments.  Every step of the path runs in the library: the host
+FIFO scheduler (``Scheduler``, backed by ``cb_schedule_step``), the paged KV
+append (``kv_append`` -> ``cb_kv_append``) and the paged attention
+(``paged_attention`` -> ``cb_paged_attention``).  PyTorch is used for device
+memory and streams only.  There is no CPU fallback: importing this package
+fails if the library has not been built
+(``python paged_attention_continuous_gb300/build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+from ._lib_loader import LIB_PATH, load_library
+
+_lib = load_library()
+
+CB_OK = 0
+CB_ERR_INVALID_ARG = 1
+CB_ERR_NO_BLOCKS = 2
+CB_ERR_CUDA = 3
+CB_ERR_UNSUPPORTED = 4
+CB_ERR_DEVICE_CHECK = 5
+CB_ERR_STATE = 6
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+
+DEVERR_BLOCK_RANGE = 0x1
+DEVERR_SLOT_RANGE = 0x2
+DEVERR_DECODE_QLEN = 0x4
+DEVERR_SEQ_RANGE = 0x8
+DEVERR_TIMEOUT = 0x10
+
+
+class CBError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"cb status {status}: {message}")
+        self.status = status
+
+
+def _check(st: int) -> int:
+    if st != CB_OK:
+        raise CBError(st, _lib.cb_last_error().decode())
+    return st
+
+
+class cb_config(ctypes.Structure):
+    _fields_ = [("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_batch_tokens", ctypes.c_int32),
+                ("max_requests_per_batch", ctypes.c_int32),
+                ("max_prefill_chunk", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32),
+                ("safety_margin", ctypes.c_float),
+                ("initial_free_list", ctypes.POINTER(ctypes.c_int32))]
+
+
+class cb_step(ctypes.Structure):
+    _fields_ = [("num_reqs", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
+                ("num_decodes", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
+                ("max_seq_len", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("req_ids", ctypes.POINTER(ctypes.c_int64)),
+                ("cu_seqlens_q", ctypes.POINTER(ctypes.c_int32)),
+                ("seq_lens", ctypes.POINTER(ctypes.c_int32)),
+                ("block_tables", ctypes.POINTER(ctypes.c_int32)),
+                ("slot_mapping", ctypes.POINTER(ctypes.c_int32)),
+                ("num_stalled", ctypes.c_int32),
+                ("stalled_ids", ctypes.POINTER(ctypes.c_int64)),
+                ("stalled_demand", ctypes.POINTER(ctypes.c_int32))]
+
+
+class cb_attention_args(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("cu_seqlens_q", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+                ("block_tables", ctypes.c_void_p),
+                ("num_reqs", ctypes.c_int32), ("num_decodes", ctypes.c_int32),
+                ("num_tokens", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
+                ("max_seq_len", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("dtype", ctypes.c_int32), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
+def _declare():
+    L = _lib
+    P = ctypes.POINTER
+    i32, i64, vp, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    L.cb_last_error.restype = ctypes.c_char_p
+    L.cb_version.restype = i32
+    L.cb_sched_create.argtypes = [P(cb_config), P(vp)]
+    L.cb_sched_destroy.argtypes = [vp]
+    L.cb_sched_destroy.restype = None
+    L.cb_add_request.argtypes = [vp, i64, i32, i32]
+    L.cb_add_running_request.argtypes = [vp, i64, i32, i32, i32]
+    L.cb_schedule_step.argtypes = [vp, P(cb_step)]
+    L.cb_step_done.argtypes = [vp, P(i32), P(P(i64))]
+    L.cb_request_slots.argtypes = [vp, i64, i32, i32, P(i32)]
+    L.cb_sched_counts.argtypes = [vp, P(i32), P(i32), P(i32)]
+    L.cb_sched_free_list.argtypes = [vp, P(i32), i32, P(i32)]
+    L.cb_kv_append.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+    L.cb_attention_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.cb_attention_workspace_size.restype = sz
+    L.cb_attention_workspace_init.argtypes = [vp, sz, vp]
+    L.cb_paged_attention.argtypes = [P(cb_attention_args), vp]
+    L.cb_attention_read_errors.argtypes = [vp, sz, vp, P(ctypes.c_uint32)]
+    for name in ("cb_sched_create", "cb_add_request", "cb_add_running_request",
+                 "cb_schedule_step", "cb_step_done", "cb_request_slots", "cb_sched_counts",
+                 "cb_sched_free_list", "cb_kv_append", "cb_attention_workspace_init",
+                 "cb_paged_attention", "cb_attention_read_errors"):
+        getattr(L, name).restype = ctypes.c_int
+
+
+_declare()
+
+
+def version() -> int:
+    return int(_lib.cb_version())
+
+
+def library():
+    """The loaded ctypes handle of libcb.so."""
+    return _lib
+
+
+# --------------------------------------------------------------- scheduler
+def _arr(ptr, n, dtype):
+    if n == 0:
+        return np.zeros(0, dtype=dtype)
+    return np.ctypeslib.as_array(ptr, shape=(n,)).astype(dtype, copy=True)
+
+
+class Scheduler:
+    """FIFO continuous-batching scheduler (C++), see ``cb_schedule_step``."""
+
+    def __init__(self, *, block_size: int, num_blocks: int, max_batch_tokens: int,
+                 max_requests_per_batch: int, max_blocks_per_seq: int,
+                 max_prefill_chunk: int = 0, safety_margin: float = 0.15,
+                 free_list: Optional[Sequence[int]] = None):
+        self.max_blocks_per_seq = int(max_blocks_per_seq)
+        cfg = cb_config(block_size, num_blocks, max_batch_tokens, max_requests_per_batch,
+                        max_prefill_chunk, max_blocks_per_seq, float(safety_margin), None)
+        keep = None
+        if free_list is not None:
+            keep = np.ascontiguousarray(np.asarray(free_list, dtype=np.int32))
+            if keep.shape != (num_blocks,):
+                raise ValueError("free_list must hold num_blocks ids")
+            cfg.initial_free_list = keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        h = ctypes.c_void_p()
+        _check(_lib.cb_sched_create(ctypes.byref(cfg), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.cb_sched_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def add_request(self, req_id: int, prompt_len: int, output_len: int) -> None:
+        _check(_lib.cb_add_request(self._h, req_id, prompt_len, output_len))
+
+    def add_running_request(self, req_id: int, prompt_len: int, output_len: int,
+                            num_cached: int) -> None:
+        _check(_lib.cb_add_running_request(self._h, req_id, prompt_len, output_len, num_cached))
+
+    def schedule_step(self) -> dict:
+        """Returns the step as numpy arrays (copies) plus 'status'
+        (0 = OK, 2 = NO_BLOCKS); other statuses raise CBError."""
+        s = cb_step()
+        st = _lib.cb_schedule_step(self._h, ctypes.byref(s))
+        if st not in (CB_OK, CB_ERR_NO_BLOCKS):
+            _check(st)
+        R, T, W = s.num_reqs, s.num_tokens, s.max_blocks_per_seq
+        return {
+            "status": int(st), "num_reqs": R, "num_tokens": T, "num_decodes": s.num_decodes,
+            "max_q_len": s.max_q_len, "max_seq_len": s.max_seq_len,
+            "req_ids": _arr(s.req_ids, R, np.int64),
+            "cu_seqlens_q": _arr(s.cu_seqlens_q, R + 1, np.int32),
+            "seq_lens": _arr(s.seq_lens, R, np.int32),
+            "block_tables": _arr(s.block_tables, R * W, np.int32).reshape(R, W),
+            "slot_mapping": _arr(s.slot_mapping, T, np.int32),
+            "stalled_ids": _arr(s.stalled_ids, s.num_stalled, np.int64),
+            "stalled_demand": _arr(s.stalled_demand, s.num_stalled, np.int32),
+        }
+
+    def step_done(self) -> list:
+        n = ctypes.c_int32()
+        ids = ctypes.POINTER(ctypes.c_int64)()
+        _check(_lib.cb_step_done(self._h, ctypes.byref(n), ctypes.byref(ids)))
+        return [int(x) for x in _arr(ids, n.value, np.int64)]
+
+    def slots(self, req_id: int, start: int, count: int) -> np.ndarray:
+        out = np.zeros(count, dtype=np.int32)
+        _check(_lib.cb_request_slots(self._h, req_id, start, count,
+                                     out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+        return out
+
+    def counts(self):
+        f, w, r = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(_lib.cb_sched_counts(self._h, ctypes.byref(f), ctypes.byref(w), ctypes.byref(r)))
+        return f.value, w.value, r.value
+
+    @property
+    def free(self) -> list:
+        n = ctypes.c_int32()
+        _check(_lib.cb_sched_free_list(self._h, None, 0, ctypes.byref(n)))
+        out = np.zeros(max(n.value, 1), dtype=np.int32)
+        _check(_lib.cb_sched_free_list(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                       n.value, ctypes.byref(n)))
+        return out[:n.value].tolist()
+
+
+# ------------------------------------------------------------------ GPU ops
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream_ptr(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must live on the GPU (no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, *, error_word=None,
+              stream=None) -> None:
+    """cb_kv_append: k_new/v_new [T, Hkv, D]; slot_mapping int32 [T];
+    caches [num_blocks, Hkv, block_size, D]."""
+    _need_cuda(k_new, v_new, slot_mapping, k_cache, v_cache)
+    T = slot_mapping.shape[0]
+    nb, hkv, bs, d = k_cache.shape
+    ew = error_word.data_ptr() if error_word is not None else None
+    _check(_lib.cb_kv_append(k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), T,
+                             k_cache.data_ptr(), v_cache.data_ptr(), nb, hkv, d, bs,
+                             _dtype_code(k_cache), ew, _stream_ptr(stream)))
+
+
+def workspace_size(num_reqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(_lib.cb_attention_workspace_size(num_reqs, num_q_heads, num_kv_heads, head_dim))
+
+
+class Workspace:
+    """Device scratch for cb_paged_attention (zeroed once on creation)."""
+
+    def __init__(self, max_reqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 device="cuda", stream=None):
+        torch = _torch()
+        self.nbytes = workspace_size(max_reqs, num_q_heads, num_kv_heads, head_dim)
+        self.max_reqs = max_reqs
+        self.buf = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.buf.data_ptr()) % 256
+        self.ptr = self.buf.data_ptr() + off
+        _check(_lib.cb_attention_workspace_init(self.ptr, self.nbytes, _stream_ptr(stream)))
+
+    def read_errors(self, stream=None) -> int:
+        bits = ctypes.c_uint32()
+        st = _lib.cb_attention_read_errors(self.ptr, self.nbytes, _stream_ptr(stream),
+                                           ctypes.byref(bits))
+        if st not in (CB_OK, CB_ERR_DEVICE_CHECK):
+            _check(st)
+        return int(bits.value)
+
+    def reinit(self, stream=None):
+        _check(_lib.cb_attention_workspace_init(self.ptr, self.nbytes, _stream_ptr(stream)))
+
+
+def paged_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens, block_tables, *,
+                    num_decodes: int, max_q_len: int, max_seq_len: int, scale: float,
+                    workspace: Workspace, out=None, stream=None):
+    """cb_paged_attention.  q [T, Hq, D]; caches [num_blocks, Hkv, bs, D];
+    metadata int32 device tensors.  Returns out [T, Hq, D]."""
+    torch = _torch()
+    _need_cuda(q, k_cache, v_cache, cu_seqlens_q, seq_lens, block_tables)
+    if out is None:
+        out = torch.empty_like(q)
+    T, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    R = seq_lens.shape[0]
+    if R > workspace.max_reqs:
+        raise ValueError("workspace sized for fewer requests")
+    a = cb_attention_args(q.data_ptr(), out.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                          cu_seqlens_q.data_ptr(), seq_lens.data_ptr(), block_tables.data_ptr(),
+                          R, num_decodes, T, max_q_len, max_seq_len, nb, block_tables.shape[1],
+                          bs, hq, hkv, d, float(scale), _dtype_code(q), workspace.ptr,
+                          workspace.nbytes)
+    _check(_lib.cb_paged_attention(ctypes.byref(a), _stream_ptr(stream)))
+    return out
+
+
+def paged_attention_args(**kw) -> cb_attention_args:
+    """Build a raw cb_attention_args (for callers that drive the C ABI
+    directly, e.g. with CUDA graphs)."""
+    return cb_attention_args(**kw)
+
+
+__all__ = ["Scheduler", "kv_append", "paged_attention", "Workspace", "workspace_size",
+           "CBError", "version", "library", "LIB_PATH"]

@@ -1,0 +1,24 @@
+// Entry points of the prefill-chunk kernel (tcgen05 tensor cores), used by
+// the attention dispatcher.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/cb.h"
+
+namespace cb {
+
+// Whether the tensor-core prefill kernel handles this GQA group size.
+bool prefill_supported(int group);
+
+// Scratch bytes the prefill kernel needs inside the attention workspace.
+size_t prefill_workspace_bytes(int64_t num_reqs, int64_t Hq, int64_t Hkv, int64_t D);
+
+// Launch the prefill-chunk kernel over rows [num_decodes, num_reqs) (bf16,
+// head_dim 128).  Returns CB_ERR_UNSUPPORTED if it cannot take this call.
+cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, uint8_t* scratch,
+                              cudaStream_t stream);
+
+}  // namespace cb

@@ -1,0 +1,369 @@
+// FIFO continuous-batching scheduler with a paged block pool (host side).
+//
+// Behaviour follows "Continuous batching architecture" (HF Transformers docs):
+//   * Request lifecycle: PENDING -> PREFILLING -> DECODING -> FINISHED; one
+//     output token per decode step.
+//   * Chunked prefill: a prompt beyond the remaining token budget is cut; the
+//     rest resumes next step where it stopped.
+//   * Scheduler: token budget (max_batch_tokens), cache budget (free blocks),
+//     request cap (max_requests_per_batch).
+//   * FIFO: running decodes first, then running prefills, then waiting
+//     requests in arrival order.
+//   * Admission: all-or-nothing allocation; safety_margin keeps new prefills
+//     out while free capacity would drop below it.
+//   * Offloading: active requests that cannot get their blocks are reported
+//     as stalled together with their block demand.
+// and the block pool of "vLLM serving internals" (PagedAttention as a virtual
+// memory system): fixed-size blocks, one block table per sequence, a new
+// block when a sequence outgrows its last one, blocks back to the pool when
+// it finishes.
+//
+// Where the pages leave a step open the choices are: batch rows in the order
+// decodes / running prefills / new prompts; strict head-of-line admission;
+// chunk = min(remaining prompt, remaining budget, max_prefill_chunk);
+// allocation only for the scheduled tokens; the free list is a FIFO queue
+// (pop from the head, finished requests push their blocks to the tail in
+// batch order and logical block order); the margin test is
+// free_after >= ceil((double)margin * num_blocks) for new requests only; the
+// step that completes a prompt yields the first output token.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <deque>
+#include <memory>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "cb_error.h"
+
+namespace cb {
+
+std::string& last_error_slot() {
+  static thread_local std::string s;
+  return s;
+}
+
+enum class State { kWaiting, kPrefilling, kDecoding, kFinished };
+
+struct Request {
+  int64_t id = 0;
+  int32_t prompt_len = 0;
+  int32_t output_len = 0;
+  int32_t num_cached = 0;     // tokens whose K/V is in the cache
+  int32_t num_generated = 0;  // output tokens produced so far
+  State state = State::kWaiting;
+  std::vector<int32_t> blocks;
+};
+
+struct Scheduled {
+  Request* req;
+  int32_t num_tokens;
+};
+
+}  // namespace cb
+
+struct cb_sched {
+  cb_config cfg{};
+  int64_t reserved_blocks = 0;
+  std::deque<int32_t> free_list;
+  std::deque<cb::Request*> waiting;
+  std::vector<cb::Request*> running;  // admission order
+  std::unordered_map<int64_t, std::unique_ptr<cb::Request>> requests;
+  bool step_open = false;
+  std::vector<cb::Scheduled> batch;
+  // step outputs (host arrays owned here)
+  std::vector<int64_t> req_ids;
+  std::vector<int32_t> cu_seqlens_q, seq_lens, block_tables, slot_mapping;
+  std::vector<int64_t> stalled_ids;
+  std::vector<int32_t> stalled_demand;
+  std::vector<int64_t> finished_ids;
+};
+
+namespace {
+
+int64_t blocks_for(const cb_sched* s, int64_t tokens) {
+  const int64_t bs = s->cfg.block_size;
+  return (tokens + bs - 1) / bs;
+}
+
+void take_blocks(cb_sched* s, cb::Request* r, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    r->blocks.push_back(s->free_list.front());
+    s->free_list.pop_front();
+  }
+}
+
+cb_status check_new_request(cb_sched* s, int64_t id, int32_t prompt_len,
+                            int32_t output_len) {
+  if (s->requests.count(id)) return cb::fail(CB_ERR_INVALID_ARG, "duplicate request id %lld", (long long)id);
+  if (prompt_len < 1 || output_len < 1)
+    return cb::fail(CB_ERR_INVALID_ARG, "prompt_len and output_len must be >= 1");
+  const int64_t longest = (int64_t)prompt_len + output_len - 1;
+  if (blocks_for(s, longest) > s->cfg.max_blocks_per_seq)
+    return cb::fail(CB_ERR_INVALID_ARG,
+                    "request %lld needs %lld blocks > max_blocks_per_seq %d", (long long)id,
+                    (long long)blocks_for(s, longest), s->cfg.max_blocks_per_seq);
+  return CB_OK;
+}
+
+void emit_step(cb_sched* s, int32_t num_decodes, cb_step* out) {
+  const int32_t R = (int32_t)s->batch.size();
+  const int32_t W = s->cfg.max_blocks_per_seq;
+  const int32_t bs = s->cfg.block_size;
+  s->req_ids.assign(R, 0);
+  s->cu_seqlens_q.assign(R + 1, 0);
+  s->seq_lens.assign(R, 0);
+  s->block_tables.assign((size_t)R * W, -1);
+  s->slot_mapping.clear();
+  int32_t max_q = 0, max_seq = 0;
+  for (int32_t i = 0; i < R; ++i) {
+    const cb::Request* r = s->batch[i].req;
+    const int32_t n = s->batch[i].num_tokens;
+    s->req_ids[i] = r->id;
+    s->cu_seqlens_q[i + 1] = s->cu_seqlens_q[i] + n;
+    s->seq_lens[i] = r->num_cached + n;
+    max_q = std::max(max_q, n);
+    max_seq = std::max(max_seq, s->seq_lens[i]);
+    std::copy(r->blocks.begin(), r->blocks.end(), s->block_tables.begin() + (size_t)i * W);
+    for (int32_t pos = r->num_cached; pos < r->num_cached + n; ++pos)
+      s->slot_mapping.push_back(r->blocks[pos / bs] * bs + pos % bs);
+  }
+  out->num_reqs = R;
+  out->num_tokens = s->cu_seqlens_q[R];
+  out->num_decodes = num_decodes;
+  out->max_q_len = max_q;
+  out->max_seq_len = max_seq;
+  out->max_blocks_per_seq = W;
+  out->req_ids = s->req_ids.data();
+  out->cu_seqlens_q = s->cu_seqlens_q.data();
+  out->seq_lens = s->seq_lens.data();
+  out->block_tables = s->block_tables.data();
+  out->slot_mapping = s->slot_mapping.data();
+  out->num_stalled = (int32_t)s->stalled_ids.size();
+  out->stalled_ids = s->stalled_ids.data();
+  out->stalled_demand = s->stalled_demand.data();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cb_last_error(void) { return cb::last_error_slot().c_str(); }
+
+int32_t cb_version(void) { return (1 << 16) | 0; }
+
+cb_status cb_sched_create(const cb_config* cfg, cb_sched** out) {
+  if (!out) return cb::fail(CB_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg) return cb::fail(CB_ERR_INVALID_ARG, "cfg is NULL");
+  if (cfg->block_size <= 0 || cfg->num_blocks <= 0 || cfg->max_batch_tokens <= 0 ||
+      cfg->max_requests_per_batch <= 0 || cfg->max_blocks_per_seq <= 0 ||
+      cfg->max_prefill_chunk < 0)
+    return cb::fail(CB_ERR_INVALID_ARG, "config sizes must be positive");
+  if (!(cfg->safety_margin >= 0.0f) || cfg->safety_margin > 1.0f)
+    return cb::fail(CB_ERR_INVALID_ARG, "safety_margin must be in [0, 1]");
+  std::unique_ptr<cb_sched> s(new (std::nothrow) cb_sched());
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "out of host memory");
+  s->cfg = *cfg;
+  s->cfg.initial_free_list = nullptr;
+  s->reserved_blocks = (int64_t)std::ceil((double)cfg->safety_margin * (double)cfg->num_blocks);
+  if (cfg->initial_free_list) {
+    std::vector<char> seen(cfg->num_blocks, 0);
+    for (int32_t i = 0; i < cfg->num_blocks; ++i) {
+      const int32_t b = cfg->initial_free_list[i];
+      if (b < 0 || b >= cfg->num_blocks || seen[b])
+        return cb::fail(CB_ERR_INVALID_ARG, "initial_free_list is not a permutation");
+      seen[b] = 1;
+      s->free_list.push_back(b);
+    }
+  } else {
+    for (int32_t i = 0; i < cfg->num_blocks; ++i) s->free_list.push_back(i);
+  }
+  *out = s.release();
+  return CB_OK;
+}
+
+void cb_sched_destroy(cb_sched* s) { delete s; }
+
+cb_status cb_add_request(cb_sched* s, int64_t req_id, int32_t prompt_len, int32_t output_len) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  cb_status st = check_new_request(s, req_id, prompt_len, output_len);
+  if (st != CB_OK) return st;
+  auto r = std::make_unique<cb::Request>();
+  r->id = req_id;
+  r->prompt_len = prompt_len;
+  r->output_len = output_len;
+  s->waiting.push_back(r.get());
+  s->requests.emplace(req_id, std::move(r));
+  return CB_OK;
+}
+
+cb_status cb_add_running_request(cb_sched* s, int64_t req_id, int32_t prompt_len,
+                                 int32_t output_len, int32_t num_cached) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  cb_status st = check_new_request(s, req_id, prompt_len, output_len);
+  if (st != CB_OK) return st;
+  if (num_cached < 0 || (int64_t)num_cached > (int64_t)prompt_len + output_len - 2)
+    return cb::fail(CB_ERR_INVALID_ARG, "num_cached must be in [0, prompt_len + output_len - 2]");
+  if (s->step_open) return cb::fail(CB_ERR_STATE, "a step is open; call cb_step_done first");
+  const int64_t need = blocks_for(s, num_cached);
+  if (need > (int64_t)s->free_list.size())
+    return cb::fail(CB_ERR_NO_BLOCKS, "not enough free blocks to resume request %lld", (long long)req_id);
+  auto r = std::make_unique<cb::Request>();
+  r->id = req_id;
+  r->prompt_len = prompt_len;
+  r->output_len = output_len;
+  r->num_cached = num_cached;
+  if (num_cached >= prompt_len) {
+    r->state = cb::State::kDecoding;
+    r->num_generated = num_cached - prompt_len + 1;
+  } else {
+    r->state = cb::State::kPrefilling;
+  }
+  take_blocks(s, r.get(), need);
+  s->running.push_back(r.get());
+  s->requests.emplace(req_id, std::move(r));
+  return CB_OK;
+}
+
+cb_status cb_schedule_step(cb_sched* s, cb_step* out) {
+  if (!s || !out) return cb::fail(CB_ERR_INVALID_ARG, "NULL argument");
+  if (s->step_open) return cb::fail(CB_ERR_STATE, "previous step not committed with cb_step_done");
+  int64_t budget = s->cfg.max_batch_tokens;
+  const size_t cap = (size_t)s->cfg.max_requests_per_batch;
+  const int64_t chunk_cap = s->cfg.max_prefill_chunk;
+  s->batch.clear();
+  s->stalled_ids.clear();
+  s->stalled_demand.clear();
+
+  // 1) running decodes, one token each
+  for (cb::Request* r : s->running) {
+    if (r->state != cb::State::kDecoding) continue;
+    if (budget == 0 || s->batch.size() == cap) break;
+    const int64_t need = blocks_for(s, (int64_t)r->num_cached + 1) - (int64_t)r->blocks.size();
+    if (need > (int64_t)s->free_list.size()) {
+      s->stalled_ids.push_back(r->id);
+      s->stalled_demand.push_back((int32_t)need);
+      continue;
+    }
+    take_blocks(s, r, need);
+    s->batch.push_back({r, 1});
+    budget -= 1;
+  }
+  const int32_t num_decodes = (int32_t)s->batch.size();
+
+  // 2) running prefills, next chunk each
+  for (cb::Request* r : s->running) {
+    if (r->state != cb::State::kPrefilling) continue;
+    if (budget == 0 || s->batch.size() == cap) break;
+    int64_t n = std::min<int64_t>(r->prompt_len - r->num_cached, budget);
+    if (chunk_cap > 0) n = std::min(n, chunk_cap);
+    const int64_t need = blocks_for(s, r->num_cached + n) - (int64_t)r->blocks.size();
+    if (need > (int64_t)s->free_list.size()) {
+      s->stalled_ids.push_back(r->id);
+      s->stalled_demand.push_back((int32_t)need);
+      continue;
+    }
+    take_blocks(s, r, need);
+    s->batch.push_back({r, (int32_t)n});
+    budget -= n;
+  }
+
+  // 3) waiting requests, arrival order, head-of-line
+  while (!s->waiting.empty() && budget > 0 && s->batch.size() < cap) {
+    cb::Request* r = s->waiting.front();
+    int64_t n = std::min<int64_t>(r->prompt_len, budget);
+    if (chunk_cap > 0) n = std::min(n, chunk_cap);
+    const int64_t need = blocks_for(s, n);
+    if ((int64_t)s->free_list.size() - need < s->reserved_blocks) break;
+    s->waiting.pop_front();
+    take_blocks(s, r, need);
+    r->state = cb::State::kPrefilling;
+    s->running.push_back(r);
+    s->batch.push_back({r, (int32_t)n});
+    budget -= n;
+  }
+
+  emit_step(s, num_decodes, out);
+  if (s->batch.empty() && (!s->stalled_ids.empty() || !s->waiting.empty())) {
+    s->step_open = false;
+    return cb::fail(CB_ERR_NO_BLOCKS, "no batch could be scheduled (%d stalled, %zu waiting)",
+                    out->num_stalled, s->waiting.size());
+  }
+  s->step_open = true;
+  return CB_OK;
+}
+
+cb_status cb_step_done(cb_sched* s, int32_t* num_finished, const int64_t** finished_ids) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  if (!s->step_open) return cb::fail(CB_ERR_STATE, "no open step");
+  s->finished_ids.clear();
+  std::vector<cb::Request*> done;
+  for (const cb::Scheduled& e : s->batch) {
+    cb::Request* r = e.req;
+    r->num_cached += e.num_tokens;
+    if (r->state == cb::State::kPrefilling) {
+      if (r->num_cached == r->prompt_len) {
+        r->num_generated = 1;
+        r->state = cb::State::kDecoding;
+      }
+    } else {
+      r->num_generated += 1;
+    }
+    if (r->state == cb::State::kDecoding && r->num_generated >= r->output_len) {
+      r->state = cb::State::kFinished;
+      done.push_back(r);
+    }
+  }
+  for (cb::Request* r : done) {
+    s->running.erase(std::find(s->running.begin(), s->running.end(), r));
+    for (int32_t b : r->blocks) s->free_list.push_back(b);
+    r->blocks.clear();
+    s->finished_ids.push_back(r->id);
+    s->requests.erase(r->id);
+  }
+  s->batch.clear();
+  s->step_open = false;
+  if (num_finished) *num_finished = (int32_t)s->finished_ids.size();
+  if (finished_ids) *finished_ids = s->finished_ids.data();
+  return CB_OK;
+}
+
+cb_status cb_request_slots(const cb_sched* s, int64_t req_id, int32_t start, int32_t count,
+                           int32_t* slots_out) {
+  if (!s || (count > 0 && !slots_out)) return cb::fail(CB_ERR_INVALID_ARG, "NULL argument");
+  auto it = s->requests.find(req_id);
+  if (it == s->requests.end()) return cb::fail(CB_ERR_INVALID_ARG, "unknown request %lld", (long long)req_id);
+  const cb::Request* r = it->second.get();
+  const int64_t bs = s->cfg.block_size;
+  if (start < 0 || count < 0 || (int64_t)start + count > (int64_t)r->blocks.size() * bs)
+    return cb::fail(CB_ERR_INVALID_ARG, "positions outside the request's blocks");
+  for (int32_t i = 0; i < count; ++i) {
+    const int64_t pos = (int64_t)start + i;
+    slots_out[i] = (int32_t)(r->blocks[pos / bs] * bs + pos % bs);
+  }
+  return CB_OK;
+}
+
+cb_status cb_sched_counts(const cb_sched* s, int32_t* free_blocks, int32_t* num_waiting,
+                          int32_t* num_running) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  if (free_blocks) *free_blocks = (int32_t)s->free_list.size();
+  if (num_waiting) *num_waiting = (int32_t)s->waiting.size();
+  if (num_running) *num_running = (int32_t)s->running.size();
+  return CB_OK;
+}
+
+cb_status cb_sched_free_list(const cb_sched* s, int32_t* out, int32_t capacity, int32_t* count) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  const int32_t n = (int32_t)s->free_list.size();
+  if (count) *count = n;
+  if (out) {
+    const int32_t m = std::min(n, capacity);
+    for (int32_t i = 0; i < m; ++i) out[i] = s->free_list[i];
+  }
+  return CB_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,148 @@
+"""Run a workload step by step through the CUDA path (C scheduler + StepRunner)
+and through the oracle (oracle scheduler + oracle append + oracle attention)
+on the same seeded inputs, and compare.
+
+Inputs: the paged pool's initial contents (context written before the
+workload starts) and every step's q/k/v come from ``workloads`` generators,
+drawn on the device.  The oracle never sees anything the CUDA kernels wrote:
+it snapshots, from a pristine copy of the initial pool, the blocks its own
+block tables reference, appends each step's new K/V itself, and attends with
+its own scheduler's metadata.  To keep full-size cases cheap the oracle can
+follow a sample of requests only; block ids are remapped into a compact
+sub-pool (paging is invisible, which the oracle's own pins establish).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import workloads
+from oracle import attention as oatt
+from oracle import paged_kv
+from tests.sched_driver import load_scenario, normalize, oracle_from_config, scenario_to_config
+
+TOL = {"f32": (1e-4, 0.0), "bf16": (2e-2, 1e-2)}
+
+
+def tolerance_ok(gpu: np.ndarray, ref: np.ndarray, dtype: str):
+    atol, rtol = TOL[dtype]
+    err = np.abs(gpu - ref)
+    bound = atol + rtol * np.abs(ref)
+    return bool((err <= bound).all()), float(err.max(initial=0.0)), float((err - bound).max(initial=-1))
+
+
+class ParityRun:
+    def __init__(self, sc, sample=None, device="cuda", fill_seed=1234, max_tokens=None):
+        import paged_attention_continuous_gb300 as cb
+        from paged_attention_continuous_gb300.step import StepRunner
+        self.sc = sc
+        self.dtype = sc.dtype
+        cfg = scenario_to_config(sc)
+        self.o = oracle_from_config(cfg)
+        self.c = cb.Scheduler(block_size=cfg["block_size"], num_blocks=cfg["num_blocks"],
+                              max_batch_tokens=cfg["max_batch_tokens"],
+                              max_requests_per_batch=cfg["max_requests_per_batch"],
+                              max_blocks_per_seq=cfg["max_blocks_per_seq"],
+                              max_prefill_chunk=cfg["max_prefill_chunk"],
+                              safety_margin=cfg["safety_margin"], free_list=cfg["free_list"])
+        load_scenario(self.o, sc)
+        load_scenario(self.c, sc)
+        self.runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
+                                 num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim,
+                                 dtype=sc.dtype, max_reqs=sc.max_requests_per_batch,
+                                 max_tokens=max_tokens or sc.max_batch_tokens,
+                                 max_blocks_per_seq=sc.max_blocks_per_seq,
+                                 num_layers=sc.num_layers, device=device)
+        self.device = device
+        self.pristine = []
+        for layer in range(sc.num_layers):
+            kp = workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size, sc.head_dim,
+                                      seed=fill_seed + 2 * layer, dtype=sc.dtype,
+                                      scale=sc.value_scale, device=device)
+            vp = workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size, sc.head_dim,
+                                      seed=fill_seed + 2 * layer + 1, dtype=sc.dtype,
+                                      scale=sc.value_scale, device=device)
+            self.runner.k_cache[layer].copy_(kp)
+            self.runner.v_cache[layer].copy_(vp)
+            self.pristine.append((kp, vp))
+        self.sample = None if sample is None else set(int(x) for x in sample)
+        # oracle sub-pool: physical block -> compact index, per layer arrays
+        self.idx = {}
+        shape = (0, sc.num_kv_heads, sc.block_size, sc.head_dim)
+        self.sub_k = [np.zeros(shape) for _ in range(sc.num_layers)]
+        self.sub_v = [np.zeros(shape) for _ in range(sc.num_layers)]
+        self.step_idx = 0
+
+    def _followed(self, rid):
+        return self.sample is None or int(rid) in self.sample
+
+    def _snapshot(self, blocks):
+        new = [int(b) for b in blocks if int(b) >= 0 and int(b) not in self.idx]
+        if not new:
+            return
+        base = len(self.idx)
+        for i, b in enumerate(new):
+            self.idx[b] = base + i
+        sel = torch.tensor(new, dtype=torch.long, device=self.device)
+        for layer, (kp, vp) in enumerate(self.pristine):
+            k = kp.index_select(0, sel).double().cpu().numpy()
+            v = vp.index_select(0, sel).double().cpu().numpy()
+            self.sub_k[layer] = np.concatenate([self.sub_k[layer], k])
+            self.sub_v[layer] = np.concatenate([self.sub_v[layer], v])
+
+    def step(self):
+        """One step on both sides.  Returns (status, gpu_out[layer] as float64
+        numpy for followed rows, oracle_out[layer], followed token indices)."""
+        sc = self.sc
+        so = self.o.schedule_step()
+        sg = self.c.schedule_step()
+        assert normalize(so) == normalize(sg), "schedulers disagree"
+        if so["status"] != 0:
+            return so["status"], None, None, None
+        T = so["num_tokens"]
+        rows = [i for i, rid in enumerate(so["req_ids"]) if self._followed(rid)]
+        toks = np.concatenate([np.arange(so["cu_seqlens_q"][i], so["cu_seqlens_q"][i + 1])
+                               for i in rows]) if rows else np.zeros(0, dtype=np.int64)
+        for i in rows:
+            self._snapshot(so["block_tables"][i])
+        ds = self.runner.upload(sg)
+        gpu_outs, ref_outs = [], []
+        bs = sc.block_size
+        for layer in range(sc.num_layers):
+            seeds = [workloads.step_seed(sc.seed, self.step_idx, layer, w) for w in range(3)]
+            q = workloads.token_tensors(T, sc.num_q_heads, sc.head_dim, seed=seeds[0], dtype=sc.dtype,
+                                        scale=sc.value_scale, device=self.device)
+            k = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[1], dtype=sc.dtype,
+                                        scale=sc.value_scale, device=self.device)
+            v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[2], dtype=sc.dtype,
+                                        scale=sc.value_scale, device=self.device)
+            # oracle inputs (copies of the generator's output, before any kernel runs)
+            sel = torch.as_tensor(toks, dtype=torch.long, device=self.device)
+            qo = q.index_select(0, sel).double().cpu().numpy()
+            ko = k.index_select(0, sel).double().cpu().numpy()
+            vo = v.index_select(0, sel).double().cpu().numpy()
+            out = self.runner.run(ds, q, k, v, layer=layer)
+            gpu_outs.append(out.index_select(0, sel).double().cpu().numpy())
+            # oracle: append followed rows' tokens into the sub-pool, then attend
+            slots = []
+            for t in toks:
+                s = int(so["slot_mapping"][t])
+                slots.append(self.idx[s // bs] * bs + s % bs)
+            paged_kv.append(self.sub_k[layer], self.sub_v[layer], ko, vo,
+                            np.asarray(slots, dtype=np.int64), bs)
+            cu = [0]
+            for i in rows:
+                cu.append(cu[-1] + int(so["cu_seqlens_q"][i + 1] - so["cu_seqlens_q"][i]))
+            bt = np.full((len(rows), so["block_tables"].shape[1]), -1, dtype=np.int64)
+            for j, i in enumerate(rows):
+                for c, b in enumerate(so["block_tables"][i]):
+                    if b >= 0:
+                        bt[j, c] = self.idx[int(b)]
+            ref = oatt.paged_attention(qo, self.sub_k[layer], self.sub_v[layer], np.asarray(cu),
+                                       so["seq_lens"][rows], bt, bs, sc.softmax_scale)
+            ref_outs.append(ref)
+        assert self.o.step_done() == self.c.step_done()
+        errs = self.runner.workspace.read_errors()
+        assert errs == 0, f"device error bits {errs:#x}"
+        self.step_idx += 1
+        return 0, gpu_outs, ref_outs, toks

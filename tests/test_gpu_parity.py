@@ -1,0 +1,271 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Bars: KV cache contents and scheduler metadata bit-exact; fp32 outputs
+max-abs <= 1e-4; bf16 outputs |gpu - oracle| <= 2e-2 + 1e-2 * |oracle|
+elementwise.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attention as oatt
+from oracle import paged_kv
+from tests.gpu_harness import ParityRun, tolerance_ok
+
+pytestmark = pytest.mark.gpu
+
+
+def _cb():
+    import paged_attention_continuous_gb300 as cb
+    return cb
+
+
+def _check(gpu, ref, dtype, what=""):
+    ok, err, excess = tolerance_ok(gpu, ref, dtype)
+    assert ok, f"{what}: max err {err:.3e}, worst excess over bound {excess:.3e}"
+    return err
+
+
+# ---------------------------------------------------------------- append
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64), ("bf16", 64)])
+def test_kv_append_bit_exact(dtype, D):
+    cb = _cb()
+    nb, Hkv, bs, T = 40, 4, 16, 77
+    rng = np.random.default_rng(3)
+    slots = rng.choice(nb * bs, size=T, replace=False).astype(np.int32)
+    slots[[5, 17, 40]] = -1
+    k0 = workloads.cache_fill(nb, Hkv, bs, D, seed=1, dtype=dtype, device="cuda")
+    v0 = workloads.cache_fill(nb, Hkv, bs, D, seed=2, dtype=dtype, device="cuda")
+    kn = workloads.token_tensors(T, Hkv, D, seed=3, dtype=dtype, device="cuda")
+    vn = workloads.token_tensors(T, Hkv, D, seed=4, dtype=dtype, device="cuda")
+    ko = k0.double().cpu().numpy(); vo = v0.double().cpu().numpy()
+    paged_kv.append(ko, vo, kn.double().cpu().numpy(), vn.double().cpu().numpy(), slots, bs)
+    kc, vc = k0.clone(), v0.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cb.kv_append(kn, vn, torch.from_numpy(slots).cuda(), kc, vc, error_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    tdt = kc.dtype
+    assert torch.equal(kc.cpu(), torch.from_numpy(ko).to(tdt))
+    assert torch.equal(vc.cpu(), torch.from_numpy(vo).to(tdt))
+
+
+def test_kv_append_out_of_range_slot_is_flagged_not_written():
+    cb = _cb()
+    nb, Hkv, bs, D = 4, 2, 16, 128
+    kc = torch.zeros(nb, Hkv, bs, D, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    kn = torch.ones(2, Hkv, D, dtype=torch.bfloat16, device="cuda")
+    slots = torch.tensor([3, nb * bs + 5], dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cb.kv_append(kn, kn, slots, kc, vc, error_word=err)
+    torch.cuda.synchronize()
+    assert err.item() == cb.DEVERR_SLOT_RANGE
+    assert kc.float().sum().item() == Hkv * D      # only slot 3 written
+
+
+# ---------------------------------------------------------------- decode
+def _decode_scenario(ctx, Hq, Hkv, D, dtype, seed=0, extra_blocks=7):
+    running = [workloads.RunningRequest(req_id=i, prompt_len=c - 1, output_len=8, num_cached=c - 1)
+               for i, c in enumerate(ctx)]
+    nb = sum(-(-c // 16) for c in ctx) + extra_blocks
+    return workloads.Scenario(
+        name="decode_edges", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, dtype=dtype,
+        num_blocks=nb, max_batch_tokens=len(ctx), max_requests_per_batch=len(ctx),
+        max_prefill_chunk=0, safety_margin=0.0, max_blocks_per_seq=0,
+        free_list=workloads.permuted_free_list(nb, seed + 5), running=running, waiting=[],
+        value_scale=0.5 if dtype == "bf16" else 1.0, seed=seed)
+
+
+EDGE_CTX = [2, 3, 15, 16, 17, 31, 32, 33, 100, 255, 256, 257, 1000, 2049]
+
+
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64), ("f32", 128), ("bf16", 64)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (32, 8), (16, 2)])
+def test_decode_edges(dtype, D, Hq, Hkv):
+    sc = _decode_scenario(EDGE_CTX, Hq, Hkv, D, dtype)
+    run = ParityRun(sc)
+    st, g, r, _ = run.step()
+    assert st == 0
+    _check(g[0], r[0], dtype, "decode")
+    # a second step (every context one longer) reuses the workspace
+    st, g, r, _ = run.step()
+    _check(g[0], r[0], dtype, "decode step 2")
+
+
+def test_decode_many_splits_and_rows():
+    ctx = list(np.random.default_rng(0).integers(2, 9000, size=70))
+    sc = _decode_scenario(ctx, 32, 8, 128, "bf16")
+    run = ParityRun(sc)
+    st, g, r, _ = run.step()
+    _check(g[0], r[0], "bf16", "decode 70 rows")
+
+
+def test_paging_invisible_on_gpu():
+    """Different physical placements of the same logical cache give
+    bit-identical GPU outputs."""
+    outs = []
+    for seed in (0, 11):
+        sc = _decode_scenario(EDGE_CTX, 32, 8, 128, "bf16", seed=0)
+        sc.free_list = workloads.permuted_free_list(sc.num_blocks, seed + 100)
+        run = ParityRun(sc)
+        # the initial pool contents follow the logical positions: rewrite the
+        # context tokens of every request identically for both placements
+        for r in sc.running:
+            slots = run.c.slots(r.req_id, 0, r.num_cached)
+            kv = workloads.token_tensors(r.num_cached, sc.num_kv_heads, sc.head_dim,
+                                         seed=1000 + r.req_id, dtype="bf16", scale=0.5, device="cuda")
+            vv = workloads.token_tensors(r.num_cached, sc.num_kv_heads, sc.head_dim,
+                                         seed=2000 + r.req_id, dtype="bf16", scale=0.5, device="cuda")
+            _cb().kv_append(kv, vv, torch.from_numpy(slots).cuda(), run.runner.k_cache[0],
+                            run.runner.v_cache[0])
+        step = run.c.schedule_step()
+        ds = run.runner.upload(step)
+        T = step["num_tokens"]
+        q = workloads.token_tensors(T, 32, 128, seed=7, dtype="bf16", scale=0.5, device="cuda")
+        k = workloads.token_tensors(T, 8, 128, seed=8, dtype="bf16", scale=0.5, device="cuda")
+        v = workloads.token_tensors(T, 8, 128, seed=9, dtype="bf16", scale=0.5, device="cuda")
+        outs.append(run.runner.run(ds, q, k, v).cpu())
+    assert torch.equal(outs[0], outs[1])
+
+
+# --------------------------------------------------------------- prefill
+def test_worked_example_fp32_chunked():
+    """The Chunked Prefill page's example through the whole path: 1000-token
+    prompt, 8 heads x 64 dims, fp32, budget 256 -> 256/256/256/232, block
+    size 16, permuted physical blocks; compared with one-shot attention."""
+    cb = _cb()
+    from paged_attention_continuous_gb300.step import StepRunner
+    q, k, v = workloads.worked_example_qkv()                 # [1, 8, 1000, 64]
+    qt = q[0].permute(1, 0, 2).contiguous()                 # [1000, 8, 64]
+    kt = k[0].permute(1, 0, 2).contiguous()
+    vt = v[0].permute(1, 0, 2).contiguous()
+    sc = workloads.chunked_prefill_1000()
+    s = cb.Scheduler(block_size=16, num_blocks=sc.num_blocks, max_batch_tokens=256,
+                     max_requests_per_batch=8, max_blocks_per_seq=sc.max_blocks_per_seq,
+                     safety_margin=0.0, free_list=sc.free_list)
+    s.add_request(0, 1000, 1)
+    runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=8, num_kv_heads=8, head_dim=64,
+                        dtype="f32", max_reqs=8, max_tokens=256,
+                        max_blocks_per_seq=sc.max_blocks_per_seq)
+    outs, chunks = [], []
+    while True:
+        st = s.schedule_step()
+        if st["num_reqs"] == 0:
+            break
+        p1 = int(st["seq_lens"][0]); n = int(st["cu_seqlens_q"][1]); p0 = p1 - n
+        chunks.append(n)
+        ds = runner.upload(st)
+        o = runner.run(ds, qt[p0:p1].cuda(), kt[p0:p1].cuda(), vt[p0:p1].cuda())
+        outs.append(o.double().cpu().numpy())
+        s.step_done()
+    assert chunks == [256, 256, 256, 232]
+    gpu = np.concatenate(outs)
+    ref = oatt.dense_causal_attention(qt.double().numpy(), kt.double().numpy(),
+                                      vt.double().numpy(), 1 / 8.0)
+    assert np.max(np.abs(gpu - ref)) <= 1e-4
+
+
+def _mixed_small(dtype="bf16", Hq=32, Hkv=8, D=128, seed=0):
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(20, 600, size=10)
+    running = [workloads.RunningRequest(i, int(c) - 1, 40, int(c) - 1) for i, c in enumerate(ctx)]
+    running.append(workloads.RunningRequest(10, 300, 4, 64))
+    waiting = [workloads.WaitingRequest(11 + i, int(p), 3)
+               for i, p in enumerate(rng.integers(1, 200, size=8))]
+    nb = 1200
+    return workloads.Scenario(
+        name="mixed_small", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, dtype=dtype,
+        num_blocks=nb, max_batch_tokens=256, max_requests_per_batch=24, max_prefill_chunk=128,
+        safety_margin=0.15, max_blocks_per_seq=0,
+        free_list=workloads.permuted_free_list(nb, seed + 1), running=running, waiting=waiting,
+        value_scale=0.5 if dtype == "bf16" else 1.0, seed=seed)
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 32, 8, 128), ("bf16", 16, 16, 128),
+                                           ("bf16", 64, 8, 128), ("f32", 8, 2, 64),
+                                           ("bf16", 8, 4, 64)])
+def test_mixed_steps_small(dtype, Hq, Hkv, D):
+    sc = _mixed_small(dtype, Hq, Hkv, D)
+    run = ParityRun(sc)
+    for step in range(5):
+        st, g, r, _ = run.step()
+        assert st == 0
+        _check(g[0], r[0], dtype, f"mixed step {step}")
+
+
+def test_prefill_chunk_of_one_and_seq_len_one():
+    """A chunk of length 1 that is not a decode, and a first chunk of 1 token
+    (seq_len 1, output must equal v[0])."""
+    waiting = [workloads.WaitingRequest(0, 1, 2), workloads.WaitingRequest(1, 17, 2),
+               workloads.WaitingRequest(2, 40, 2)]
+    sc = workloads.Scenario(
+        name="tiny", num_q_heads=8, num_kv_heads=2, head_dim=128, dtype="bf16",
+        num_blocks=64, max_batch_tokens=18, max_requests_per_batch=4, max_prefill_chunk=0,
+        safety_margin=0.0, max_blocks_per_seq=0, free_list=workloads.permuted_free_list(64, 2),
+        running=[], waiting=waiting, value_scale=0.5)
+    run = ParityRun(sc)
+    for _ in range(4):
+        st, g, r, _ = run.step()
+        if st != 0 or g[0].shape[0] == 0:
+            break
+        _check(g[0], r[0], "bf16", "tiny prefill")
+
+
+# ------------------------------------------------------- full-size configs
+def test_full_decode_64_sampled():
+    sc = workloads.decode_64()
+    run = ParityRun(sc, sample=[0, 1, 17, 33, 62, 63])
+    st, g, r, toks = run.step()
+    assert st == 0 and len(toks) == 6
+    _check(g[0], r[0], "bf16", "decode_64")
+
+
+def test_full_mixed_2048_sampled():
+    sc = workloads.mixed_2048()
+    sample = [0, 5, 50, 95, 96, 97, 98]     # decodes, the in-flight prefill, new prompts
+    run = ParityRun(sc, sample=sample)
+    st, g, r, toks = run.step()
+    assert st == 0
+    _check(g[0], r[0], "bf16", "mixed_2048")
+    st, g, r, toks = run.step()
+    _check(g[0], r[0], "bf16", "mixed_2048 step 2")
+
+
+def test_full_long_prompt_late_step_sampled():
+    """Long-prompt interleave at full shape (64 Q / 8 KV heads, 128 decodes);
+    steps 0..5 run, the oracle follows 3 decodes and the long prompt."""
+    sc = workloads.long_prompt_32k()
+    run = ParityRun(sc, sample=[0, 64, 127, 128])
+    for step in range(6):
+        st, g, r, toks = run.step()
+        assert st == 0
+    _check(g[0], r[0], "bf16", "long prompt step 6")
+
+
+def test_empty_batch_is_a_noop():
+    cb = _cb()
+    ws = cb.Workspace(4, 8, 8, 128)
+    a = cb.cb_attention_args()
+    a.num_reqs = 0
+    assert cb.library().cb_paged_attention(__import__("ctypes").byref(a), None) == 0
+
+
+def test_bad_block_id_is_flagged_not_read():
+    cb = _cb()
+    sc = _decode_scenario([40, 50], 8, 2, 128, "bf16")
+    run = ParityRun(sc)
+    step = run.c.schedule_step()
+    step["block_tables"][1, 1] = sc.num_blocks + 7        # corrupt one entry
+    ds = run.runner.upload(step)
+    T = step["num_tokens"]
+    q = torch.zeros(T, 8, 128, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(T, 2, 128, dtype=torch.bfloat16, device="cuda")
+    run.runner.run(ds, q, kv, kv)
+    bits = run.runner.workspace.read_errors()
+    assert bits & cb.DEVERR_BLOCK_RANGE
+    run.runner.workspace.reinit()
+    torch.cuda.synchronize()

@@ -251,7 +251,10 @@ typedef struct cb_attention_args {
 #define CB_DEVERR_SEQ_RANGE 0x8u    /* seq_len < q_len or beyond the table */
 #define CB_DEVERR_TIMEOUT 0x10u     /* a bounded wait ran out */
 
-/* Workspace bytes for a call with these sizes (upper bound; 0 on bad args). */
+/* Workspace bytes for calls with up to num_reqs rows and these head sizes
+ * (0 on bad args).  One workspace serves any later call with at most that
+ * many rows and the same head sizes; the regions that carry state between
+ * calls sit at fixed offsets.  num_kv_heads <= 64. */
 size_t cb_attention_workspace_size(int32_t num_reqs, int32_t num_q_heads,
                                    int32_t num_kv_heads, int32_t head_dim);
 

@@ -22,20 +22,28 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t header = 0, tickets = 0, part_ml = 0, part_acc = 0, prefill = 0, total = 0;
+  size_t header = 0, tickets = 0, prefill = 0, part_ml = 0, part_acc = 0, total = 0;
 };
 
-// header words: [0] device error bits, [1] decode item counter,
-//               [2] prefill item counter
+// Workspace regions.  The header, the decode tickets and the prefill region
+// hold state that must read zero at the start of every call (each call leaves
+// them zero), so they sit at FIXED offsets that do not depend on the call's
+// sizes.  The split partials are scratch rewritten by every call, sized by
+// the call's decode rows.
+//   header words: [0] device error bits, [1] decode item counter,
+//                 [2] prefill item counter
+constexpr int64_t kMaxKvHeads = 64;
+constexpr size_t kTicketBytes = (size_t)decode::kPlanMax * kMaxKvHeads * 4;
+
 WsLayout ws_layout(int64_t num_reqs, int64_t Hq, int64_t Hkv, int64_t D) {
   WsLayout w;
   const int64_t rows = num_reqs < decode::kPlanMax ? num_reqs : decode::kPlanMax;
   w.header = 0;
-  w.tickets = align_up(kAlign);
-  w.part_ml = w.tickets + align_up((size_t)rows * Hkv * 4);
+  w.tickets = kAlign;
+  w.prefill = w.tickets + align_up(kTicketBytes);
+  w.part_ml = w.prefill + align_up(prefill_workspace_bytes(Hq, Hkv, D));
   w.part_acc = w.part_ml + align_up((size_t)rows * decode::kMaxSplits * Hq * 2 * 4);
-  w.prefill = w.part_acc + align_up((size_t)rows * decode::kMaxSplits * Hq * D * 4);
-  w.total = w.prefill + align_up(prefill_workspace_bytes(num_reqs, Hq, Hkv, D));
+  w.total = w.part_acc + align_up((size_t)rows * decode::kMaxSplits * Hq * D * 4);
   return w;
 }
 
@@ -199,6 +207,8 @@ extern "C" cb_status cb_paged_attention(const cb_attention_args* args, cb_stream
   if (a.num_tokens < a.num_reqs) return fail(CB_ERR_INVALID_ARG, "num_tokens < num_reqs");
   if (a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.num_q_heads % a.num_kv_heads != 0)
     return fail(CB_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (a.num_kv_heads > cb::kMaxKvHeads)
+    return fail(CB_ERR_UNSUPPORTED, "num_kv_heads > %d", (int)cb::kMaxKvHeads);
   if (a.block_size != 16) return fail(CB_ERR_UNSUPPORTED, "block_size must be 16");
   if (a.head_dim != 64 && a.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (a.dtype != CB_DTYPE_F32 && a.dtype != CB_DTYPE_BF16) return fail(CB_ERR_INVALID_ARG, "unknown dtype");

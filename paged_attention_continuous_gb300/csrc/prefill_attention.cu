@@ -6,7 +6,7 @@ namespace cb {
 
 bool prefill_supported(int) { return false; }
 
-size_t prefill_workspace_bytes(int64_t, int64_t, int64_t, int64_t) { return 0; }
+size_t prefill_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 
 cb_status launch_prefill_bf16(const cb_attention_args&, uint32_t*, uint8_t*, cudaStream_t) {
   return CB_ERR_UNSUPPORTED;

@@ -13,8 +13,9 @@ namespace cb {
 // Whether the tensor-core prefill kernel handles this GQA group size.
 bool prefill_supported(int group);
 
-// Scratch bytes the prefill kernel needs inside the attention workspace.
-size_t prefill_workspace_bytes(int64_t num_reqs, int64_t Hq, int64_t Hkv, int64_t D);
+// Bytes of the prefill kernel's region of the attention workspace (state
+// that must read zero between calls; independent of the call's sizes).
+size_t prefill_workspace_bytes(int64_t Hq, int64_t Hkv, int64_t D);
 
 // Launch the prefill-chunk kernel over rows [num_decodes, num_reqs) (bf16,
 // head_dim 128).  Returns CB_ERR_UNSUPPORTED if it cannot take this call.

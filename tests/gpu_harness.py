@@ -96,6 +96,7 @@ class ParityRun:
         sc = self.sc
         so = self.o.schedule_step()
         sg = self.c.schedule_step()
+        self.last = so
         assert normalize(so) == normalize(sg), "schedulers disagree"
         if so["status"] != 0:
             return so["status"], None, None, None

@@ -269,3 +269,34 @@ def test_bad_block_id_is_flagged_not_read():
     assert bits & cb.DEVERR_BLOCK_RANGE
     run.runner.workspace.reinit()
     torch.cuda.synchronize()
+
+
+def test_workspace_reused_across_calls_of_different_sizes():
+    """One workspace serves calls with different row counts: a decode-only
+    call with few rows, then the full mixed step, must give the same bytes as
+    the full step on a fresh workspace."""
+    cb = _cb()
+    sc = _mixed_small("bf16", 16, 16, 128)
+    run = ParityRun(sc)
+    st = run.c.schedule_step()
+    ds = run.runner.upload(st)
+    T, nd = st["num_tokens"], st["num_decodes"]
+    q = workloads.token_tensors(T, 16, 128, seed=1, dtype="bf16", scale=0.5, device="cuda")
+    k = workloads.token_tensors(T, 16, 128, seed=2, dtype="bf16", scale=0.5, device="cuda")
+    kc, vc = run.runner.k_cache[0], run.runner.v_cache[0]
+    cb.kv_append(k, k, ds.slot_mapping, kc, vc)
+    kw = dict(scale=0.0884, out=None)
+    full = dict(num_decodes=nd, max_q_len=st["max_q_len"], max_seq_len=st["max_seq_len"])
+    ws = run.runner.workspace
+    for n in (3, nd):
+        cb.paged_attention(q[:n], kc, vc, ds.cu_seqlens_q[:n + 1], ds.seq_lens[:n],
+                           ds.block_tables[:n], num_decodes=n, max_q_len=1,
+                           max_seq_len=int(st["seq_lens"][:n].max()), workspace=ws, **kw)
+    a = cb.paged_attention(q, kc, vc, ds.cu_seqlens_q, ds.seq_lens, ds.block_tables,
+                           workspace=ws, **full, **kw)
+    fresh = cb.Workspace(sc.max_requests_per_batch, 16, 16, 128)
+    b = cb.paged_attention(q, kc, vc, ds.cu_seqlens_q, ds.seq_lens, ds.block_tables,
+                           workspace=fresh, **full, **kw)
+    torch.cuda.synchronize()
+    assert ws.read_errors() == 0
+    assert torch.equal(a, b)

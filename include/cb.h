@@ -270,6 +270,44 @@ cb_status cb_paged_attention(const cb_attention_args* args, cb_stream_t stream);
 cb_status cb_attention_read_errors(void* workspace, size_t workspace_bytes,
                                    cb_stream_t stream, uint32_t* bits);
 
+/* ------------------------------------------------------------------------
+ * cb_paged_decode_noalloc (GPU).  No counterpart in the pages: an extra
+ * entry point for callers that cannot allocate device memory.
+ *
+ * Some callers cannot call cudaMalloc at the point where they run attention:
+ * code embedded in a host framework that owns the whole device-memory
+ * budget and forbids side allocations while it executes (a serving-engine
+ * plugin called from the framework's enqueue path, for instance), or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device
+ * synchronisation.  This call runs the same split-KV decode kernel as
+ * cb_paged_attention but takes no workspace: its scratch (split partials,
+ * tickets, work counter) lives in a fixed array of CB_NOALLOC_SCRATCH_BYTES
+ * inside this library, which every GPU that loads the library keeps until
+ * the process exits.  It allocates nothing and calls no allocating routine.
+ *
+ *   args        as for cb_paged_attention, but EVERY row must be a decode
+ *               (num_decodes == num_reqs == num_tokens, at most 1024 rows);
+ *               args->workspace and args->workspace_bytes are ignored.
+ *   error_word  optional device uint32 that receives CB_DEVERR_* bits
+ *               (NULL: device-side errors are not reported).
+ *   stream      the stream to run on.
+ *
+ * Limits: the scratch needed for the call, about
+ * num_reqs * 32 * num_q_heads * (head_dim + 2) * 4 bytes, must fit in
+ * CB_NOALLOC_SCRATCH_BYTES; larger calls are rejected with
+ * CB_ERR_INVALID_ARG and a message giving the sizes.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * Every call clears the counter and tickets it needs, then uses the array;
+ * all calls in the process share it, so calls that may overlap on the GPU
+ * (different streams without ordering between them) race with each other.
+ * ---------------------------------------------------------------------- */
+#define CB_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+cb_status cb_paged_decode_noalloc(const cb_attention_args* args, uint32_t* error_word,
+                                  cb_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,164 @@
+// cb_paged_decode_noalloc: the split-KV decode kernel with its scratch in a
+// fixed device array that this library owns, for callers that cannot
+// allocate device memory.
+//
+// Who needs it: code that runs inside a host framework which owns the whole
+// device-memory budget and does not allow side allocations while it
+// executes (an inference-server plugin called from the framework's enqueue
+// path, for example), and latency-critical loops where a cudaMalloc, with
+// its implicit device synchronisation, is not acceptable.  Such callers can
+// hand over their inputs and outputs but not a workspace.
+//
+// The scratch -- split partials (m, l, acc), per-(row, KV head) tickets, the
+// work counter -- lives in one file-scope __device__ array of
+// kNoAllocScratchBytes.  Every GPU that loads the library holds that array
+// until the process exits.  Host code must not use the array's name as a
+// device address (on the host it is only a stand-in); the device address is
+// fetched once per device with cudaGetSymbolAddress, with that device
+// current, on the first call made on that device.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "cb_error.h"
+#include "decode_attention.cuh"
+
+namespace cb {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = CB_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_decode_scratch[kNoAllocScratchBytes];
+
+struct NoAllocLayout {
+  size_t tickets = 0, part_ml = 0, part_acc = 0, total = 0, zeroed = 0;
+};
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+NoAllocLayout noalloc_layout(int64_t rows, int64_t Hq, int64_t Hkv, int64_t D) {
+  NoAllocLayout l;
+  l.tickets = 256;  // [0, 256): error word (unused here), work counter
+  l.part_ml = l.tickets + up256((size_t)rows * Hkv * 4);
+  l.part_acc = l.part_ml + up256((size_t)rows * decode::kMaxSplits * Hq * 2 * 4);
+  l.total = l.part_acc + up256((size_t)rows * decode::kMaxSplits * Hq * D * 4);
+  l.zeroed = l.part_ml;  // header + tickets must read zero when a launch starts
+  return l;
+}
+
+std::mutex g_mu;
+uint8_t* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set up once).
+cb_status scratch_for_current_device(uint8_t** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(CB_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(CB_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(CB_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return CB_OK;
+}
+
+template <typename T, int D, int G>
+cb_status launch(const cb_attention_args& a, uint8_t* scratch, const NoAllocLayout& L,
+                 uint32_t* error_word, cudaStream_t stream) {
+  constexpr int kStages = 2;
+  using WS8 = decode::WarpSmem<T, D, G, kStages>;
+  constexpr int kWarps = sizeof(WS8) * 8 + (decode::kPlanMax + 1) * 4 <= 200 * 1024 ? 8 : 4;
+  const size_t smem = sizeof(WS8) * kWarps + (decode::kPlanMax + 1) * 4;
+  auto kern = decode::decode_kernel<T, D, G, kWarps, kStages>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return fail(CB_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  decode::Params p{};
+  p.q = a.q;
+  p.out = a.out;
+  p.k_cache = a.k_cache;
+  p.v_cache = a.v_cache;
+  p.cu_seqlens_q = a.cu_seqlens_q;
+  p.seq_lens = a.seq_lens;
+  p.block_tables = a.block_tables;
+  p.row_begin = 0;
+  p.num_rows = a.num_decodes;
+  p.num_tokens = a.num_tokens;
+  p.num_blocks = a.num_blocks;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.error_word = error_word;
+  p.work_counter = reinterpret_cast<uint32_t*>(scratch) + 1;
+  p.tickets = reinterpret_cast<uint32_t*>(scratch + L.tickets);
+  p.part_ml = reinterpret_cast<float*>(scratch + L.part_ml);
+  p.part_acc = reinterpret_cast<float*>(scratch + L.part_acc);
+  kern<<<sms > 0 ? sms : 152, kWarps * 32, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(CB_ERR_CUDA, "decode kernel launch: %s", cudaGetErrorString(e));
+  return CB_OK;
+}
+
+template <typename T>
+cb_status dispatch(const cb_attention_args& a, uint8_t* s, const NoAllocLayout& L, uint32_t* ew,
+                   cudaStream_t st) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+#define CB_NA(DD, GG) \
+  if (a.head_dim == DD && G == GG) return launch<T, DD, GG>(a, s, L, ew, st);
+  CB_NA(128, 1) CB_NA(128, 2) CB_NA(128, 4) CB_NA(128, 8)
+  CB_NA(64, 1) CB_NA(64, 2) CB_NA(64, 4) CB_NA(64, 8)
+#undef CB_NA
+  return fail(CB_ERR_UNSUPPORTED, "no-alloc decode: head_dim %d with %d query heads per KV head",
+              a.head_dim, G);
+}
+
+}  // namespace
+}  // namespace cb
+
+extern "C" cb_status cb_paged_decode_noalloc(const cb_attention_args* args, uint32_t* error_word,
+                                             cb_stream_t stream_) {
+  using cb::fail;
+  if (!args) return fail(CB_ERR_INVALID_ARG, "args is NULL");
+  const cb_attention_args& a = *args;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (a.num_reqs < 0 || a.num_decodes != a.num_reqs || a.num_tokens != a.num_reqs)
+    return fail(CB_ERR_INVALID_ARG,
+                "no-alloc decode: every row must be a decode (num_decodes == num_reqs == num_tokens)");
+  if (a.num_reqs == 0) return CB_OK;
+  if (!a.q || !a.out || !a.k_cache || !a.v_cache || !a.cu_seqlens_q || !a.seq_lens || !a.block_tables)
+    return fail(CB_ERR_INVALID_ARG, "NULL pointer argument");
+  if (a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.num_q_heads % a.num_kv_heads != 0)
+    return fail(CB_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (a.block_size != 16) return fail(CB_ERR_UNSUPPORTED, "block_size must be 16");
+  if (a.dtype != CB_DTYPE_F32 && a.dtype != CB_DTYPE_BF16) return fail(CB_ERR_INVALID_ARG, "unknown dtype");
+  if (a.num_blocks <= 0 || a.max_blocks_per_seq <= 0) return fail(CB_ERR_INVALID_ARG, "bad pool sizes");
+  const uintptr_t al = (uintptr_t)a.q | (uintptr_t)a.out | (uintptr_t)a.k_cache | (uintptr_t)a.v_cache;
+  if (al & 15u) return fail(CB_ERR_INVALID_ARG, "q/out/cache pointers must be 16-byte aligned");
+  if (a.num_reqs > cb::decode::kPlanMax)
+    return fail(CB_ERR_INVALID_ARG, "no-alloc decode: at most %d rows per call", cb::decode::kPlanMax);
+  const cb::NoAllocLayout L =
+      cb::noalloc_layout(a.num_reqs, a.num_q_heads, a.num_kv_heads, a.head_dim);
+  if (L.total > cb::kNoAllocScratchBytes)
+    return fail(CB_ERR_INVALID_ARG,
+                "no-alloc decode: %d rows x %d query heads x head_dim %d need %zu scratch bytes, "
+                "more than the fixed %zu",
+                a.num_reqs, a.num_q_heads, a.head_dim, L.total, cb::kNoAllocScratchBytes);
+  uint8_t* scratch = nullptr;
+  cb_status st = cb::scratch_for_current_device(&scratch);
+  if (st != CB_OK) return st;
+  // the array keeps the previous call's contents: the counter and tickets
+  // must read zero when the kernel starts
+  cudaError_t e = cudaMemsetAsync(scratch, 0, L.zeroed, stream);
+  if (e != cudaSuccess) return fail(CB_ERR_CUDA, "clearing scratch: %s", cudaGetErrorString(e));
+  return a.dtype == CB_DTYPE_BF16 ? cb::dispatch<__nv_bfloat16>(a, scratch, L, error_word, stream)
+                                  : cb::dispatch<float>(a, scratch, L, error_word, stream);
+}

@@ -177,6 +177,20 @@ def _sub_step(step, lo, hi):
     return sub
 
 
+def time_each(torch, fn, iters, stream):
+    """Sum of per-launch device times: an event pair around every call, so
+    host-side gaps between calls are not counted."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / 1e3
+
+
 def time_loop(torch, fn, iters, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -187,6 +201,136 @@ def time_loop(torch, fn, iters, stream):
     end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / 1e3  # seconds
+
+
+def attn_call(cb, torch, dev, sc, sub, q, out, kc, vc, ws):
+    """A closure calling cb_paged_attention on a stand-alone step ``sub``
+    whose query rows are ``q``; metadata is uploaded once, here."""
+    if sub["num_reqs"] == 0:
+        return None
+    cu = torch.from_numpy(np.asarray(sub["cu_seqlens_q"], dtype=np.int32)).to(dev)
+    sl = torch.from_numpy(np.asarray(sub["seq_lens"], dtype=np.int32)).to(dev)
+    bt = torch.from_numpy(np.ascontiguousarray(sub["block_tables"], dtype=np.int32)).to(dev)
+
+    def f():
+        cb.paged_attention(q, kc, vc, cu, sl, bt, num_decodes=sub["num_decodes"],
+                           max_q_len=sub["max_q_len"], max_seq_len=sub["max_seq_len"],
+                           scale=sc.softmax_scale, workspace=ws, out=out)
+    return f
+
+
+def _runner_for(sc, dev, torch):
+    from paged_attention_continuous_gb300.step import StepRunner
+    runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
+                        num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim, dtype=sc.dtype,
+                        max_reqs=sc.max_requests_per_batch, max_tokens=sc.max_batch_tokens,
+                        max_blocks_per_seq=sc.max_blocks_per_seq, zero_cache=False)
+    runner.k_cache[0].copy_(workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size,
+                                                 sc.head_dim, seed=1234, dtype=sc.dtype,
+                                                 scale=sc.value_scale, device=dev))
+    runner.v_cache[0].copy_(workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size,
+                                                 sc.head_dim, seed=1235, dtype=sc.dtype,
+                                                 scale=sc.value_scale, device=dev))
+    return runner
+
+
+def _qkv(sc, T, dev, step=0):
+    seeds = [workloads.step_seed(sc.seed, step, 0, w) for w in range(3)]
+    mk = lambda n, s_: workloads.token_tensors(T, n, sc.head_dim, seed=s_, dtype=sc.dtype,
+                                               scale=sc.value_scale, device=dev)
+    return mk(sc.num_q_heads, seeds[0]), mk(sc.num_kv_heads, seeds[1]), mk(sc.num_kv_heads, seeds[2])
+
+
+def measure_decode_only(cb, torch, dev, reps, hbm):
+    """Decode-only step: 64 requests, contexts U[128, 4096], 32/8 heads,
+    D = 128, 20,000-block pool.  Decode kernel GB/s vs HBM peak."""
+    sc = workloads.decode_64()
+    sched = load_c_scheduler(cb, sc)
+    step = sched.schedule_step()
+    runner = _runner_for(sc, dev, torch)
+    T = step["num_tokens"]
+    q, k, v = _qkv(sc, T, dev)
+    out = torch.empty_like(q)
+    ds = runner.upload(step)
+    kc, vc = runner.k_cache[0], runner.v_cache[0]
+    runner.run(ds, q, k, v, out=out)
+    f = attn_call(cb, torch, dev, sc, step, q, out, kc, vc, runner.workspace)
+    for _ in range(5):
+        f()
+    t = time_each(torch, f, reps, torch.cuda.current_stream()) / reps
+    nbytes = decode_bytes(step, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, 2)
+    assert runner.workspace.read_errors() == 0
+    gbs = nbytes / t / 1e9
+    del runner
+    torch.cuda.empty_cache()
+    return {"workload": "decode_64 (64 decodes, ctx U[128,4096], 32Q/8KV, D=128)",
+            "kernel": "decode_kernel", "achieved_gbs": round(gbs, 1), "peak_gbs": hbm,
+            "frac": round(gbs / hbm, 4), "ms_per_launch": round(t * 1e3, 4),
+            "algorithmic_bytes_per_launch": nbytes, "launches_timed": reps}
+
+
+def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
+    """Long-prompt interleave: a 32,768-token prompt prefilled in 512-token
+    chunks over 64 scheduler steps while 128 requests decode (64 Q / 8 KV
+    heads, D = 128, budget 640).  Every step's append + attention is timed,
+    and its prefill and decode launches separately."""
+    sc = workloads.long_prompt_32k()
+    sched = load_c_scheduler(cb, sc)
+    runner = _runner_for(sc, dev, torch)
+    kc, vc = runner.k_cache[0], runner.v_cache[0]
+    ws = runner.workspace
+    stream = torch.cuda.current_stream()
+    q, k, v = _qkv(sc, sc.max_batch_tokens, dev)
+    out = torch.empty_like(q)
+    tot = {"tokens": 0, "t_step": 0.0, "t_pre": 0.0, "t_dec": 0.0, "flops": 0, "bytes": 0}
+    per_step = []
+    steps = 0
+    while steps < 64:
+        st = sched.schedule_step()
+        if st["status"] != 0 or st["num_reqs"] == 0:
+            break
+        T, R, nd = st["num_tokens"], st["num_reqs"], st["num_decodes"]
+        ds = runner.upload(st)
+        qs, ks, vs, os_ = q[:T], k[:T], v[:T], out[:T]
+        full = lambda: runner.run(ds, qs, ks, vs, out=os_)
+        dsub, psub = _sub_step(st, 0, nd), _sub_step(st, nd, R)
+        fd = attn_call(cb, torch, dev, sc, dsub, q[:nd], out[:nd], kc, vc, ws)
+        fp = attn_call(cb, torch, dev, sc, psub, q[nd:T], out[nd:T], kc, vc, ws)
+        full()
+        if fd:
+            fd()
+        if fp:
+            fp()
+        t_step = time_each(torch, full, reps, stream) / reps
+        t_dec = time_each(torch, fd, reps, stream) / reps if fd else 0.0
+        t_pre = time_each(torch, fp, reps, stream) / reps if fp else 0.0
+        fl = prefill_flops(st, sc.num_q_heads, sc.head_dim)
+        by = decode_bytes(st, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, 2)
+        tot["tokens"] += T; tot["t_step"] += t_step; tot["t_pre"] += t_pre
+        tot["t_dec"] += t_dec; tot["flops"] += fl; tot["bytes"] += by
+        if steps in (0, 16, 32, 48, 63):
+            per_step.append({"step": steps, "chunk_start": int(st["seq_lens"][-1]) - int(
+                np.diff(st["cu_seqlens_q"])[-1]), "prefill_tflops": round(fl / t_pre / 1e12, 1) if t_pre else 0,
+                "decode_gbs": round(by / t_dec / 1e9, 1) if t_dec else 0,
+                "ms_step": round(t_step * 1e3, 4)})
+        sched.step_done()
+        steps += 1
+    assert ws.read_errors() == 0
+    del runner
+    torch.cuda.empty_cache()
+    pt = tot["flops"] / tot["t_pre"] / 1e12 if tot["t_pre"] else 0.0
+    dg = tot["bytes"] / tot["t_dec"] / 1e9 if tot["t_dec"] else 0.0
+    return {"workload": "long_prompt_32k (32K prompt in 512-token chunks, 128 decodes, 64Q/8KV, D=128)",
+            "steps": steps, "tokens_per_s": round(tot["tokens"] / tot["t_step"], 1),
+            "ms_per_step": round(tot["t_step"] / max(steps, 1) * 1e3, 4),
+            "prefill": {"kernel": "prefill_kernel (tcgen05)", "achieved_tflops": round(pt, 1),
+                        "peak_tflops": bf16, "frac": round(pt / bf16, 4),
+                        "frac_sustained": round(pt / bf16s, 4),
+                        "algorithmic_flops": int(tot["flops"]),
+                        "ms_total": round(tot["t_pre"] * 1e3, 3)},
+            "decode": {"kernel": "decode_kernel", "achieved_gbs": round(dg, 1), "peak_gbs": hbm,
+                       "frac": round(dg / hbm, 4)},
+            "sampled_steps": per_step, "reps_per_step": reps}
 
 
 # ----------------------------------------------------------- CPU oracle
@@ -309,8 +453,8 @@ def run_ours(args, rank, world):
     clocks.start()
     time.sleep(0.3)
     t_step = time_loop(torch, full_step, K, stream)
-    t_dec = time_loop(torch, dec_fn, K, stream) if dec_fn else 0.0
-    t_pre = time_loop(torch, pre_fn, K, stream) if pre_fn else 0.0
+    t_dec = time_each(torch, dec_fn, K, stream) if dec_fn else 0.0
+    t_pre = time_each(torch, pre_fn, K, stream) if pre_fn else 0.0
     clk = clocks.stop()
     if world > 1:
         tt = torch.tensor([t_step], device=dev)
@@ -400,6 +544,9 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "gpu_launches": int(launches),
     }
+    if not args.no_extra:
+        line["decode_only"] = measure_decode_only(cb, torch, dev, max(K, 20), hbm)
+        line["long_prompt"] = measure_long_prompt(cb, torch, dev, 3, hbm, bf16, bf16s)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sc, step, runner, q, k, v, torch, dev,
                                             budget_s=args.cpu_seconds)
@@ -418,11 +565,16 @@ def _pristine_blocks(sc, blocks, dev, torch):
     return k, v
 
 
-def cpu_baseline(sc, step, runner, q, k, v, torch, dev, budget_s=20.0, impl_line=False):
-    """The oracle, as it stands, on a bounded sample of the step: a spread of
-    decode rows plus the prefill rows (their last queries), timed on the host
-    cores."""
-    dec_rows, pre_rows = choose_oracle_rows(step, 16)
+def cpu_baseline(sc, step, runner, q, k, v, torch, dev, budget_s=20.0, full=True):
+    """The oracle, as it stands, timed on the host cores on the step's rows:
+    all decode rows and all prefill rows, repeated until about ``budget_s``
+    seconds have passed (``full``); or, when a whole pass would not fit the
+    budget, a spread of decode rows plus each prefill row's last queries."""
+    if full:
+        dec_rows, pre_rows = list(range(step["num_decodes"])), list(range(step["num_decodes"],
+                                                                          step["num_reqs"]))
+    else:
+        dec_rows, pre_rows = choose_oracle_rows(step, 16)
     rows = dec_rows + pre_rows
     blocks = sorted({int(b) for r in rows for b in step["block_tables"][r] if b >= 0})
     kpool, vpool = _pristine_blocks(sc, blocks, dev, torch)
@@ -438,25 +590,33 @@ def cpu_baseline(sc, step, runner, q, k, v, torch, dev, budget_s=20.0, impl_line
                                      int(s) % sc.block_size if (int(s) // sc.block_size) in remap
                                      else -1 for s in step["slot_mapping"]], dtype=np.int64)
     pools = (kpool, vpool, k.float().cpu().numpy(), v.float().cpu().numpy(), q.float().cpu().numpy())
-    # size the prefill slice so one sample takes about budget_s
-    n, t = oracle_sample(sc, st, pools, dec_rows)
-    cap = 64
-    n2, t2 = oracle_sample(sc, st, pools, pre_rows, prefill_token_cap=cap)
-    per_tok = t2 / max(n2, 1)
-    room = max(budget_s - t, 0.5)
-    cap = int(max(16, min(2048, room / max(per_tok, 1e-6) / max(len(pre_rows), 1))))
-    n2, t2 = oracle_sample(sc, st, pools, pre_rows, prefill_token_cap=cap)
+    if full:
+        n_tot, t_tot, passes = 0, 0.0, 0
+        while passes == 0 or t_tot < budget_s:
+            n, t = oracle_sample(sc, st, pools, rows)
+            n_tot += n; t_tot += t; passes += 1
+        desc = (f"{sc.name} step 0: all {len(dec_rows)} decode rows and {len(pre_rows)} prefill rows "
+                f"({n} query tokens) x {passes} passes, numpy float64")
+    else:
+        n, t = oracle_sample(sc, st, pools, dec_rows)
+        cap = 64
+        n2, t2 = oracle_sample(sc, st, pools, pre_rows, prefill_token_cap=cap)
+        per_tok = t2 / max(n2, 1)
+        room = max(budget_s - t, 0.05)
+        cap = int(max(16, min(2048, room / max(per_tok, 1e-6) / max(len(pre_rows), 1))))
+        n2, t2 = oracle_sample(sc, st, pools, pre_rows, prefill_token_cap=cap)
+        n_tot, t_tot = n + n2, t + t2
+        desc = (f"{sc.name} step 0: {len(dec_rows)} of {step['num_decodes']} decode rows "
+                f"+ the last {cap} queries of each of {len(pre_rows)} prefill rows "
+                f"({n_tot} query tokens), numpy float64")
     try:
         import threadpoolctl
         threads = max(p.get("num_threads", 1) for p in threadpoolctl.threadpool_info())
     except Exception:
         threads = os.cpu_count()
-    return {"value": round((n + n2) / (t + t2), 2), "unit": "tokens/s",
-            "cores": int(threads), "host_cpus": os.cpu_count(), "kind": "oracle",
-            "seconds": round(t + t2, 2),
-            "sample": f"{sc.name} step 0: {len(dec_rows)} of {step['num_decodes']} decode rows "
-                      f"+ the last {cap} queries of each of {len(pre_rows)} prefill rows "
-                      f"({n + n2} query tokens), numpy float64"}
+    return {"value": round(n_tot / t_tot, 2), "unit": "tokens/s", "cores": int(threads),
+            "host_cpus": os.cpu_count(), "kind": "oracle", "seconds": round(t_tot, 2),
+            "sample": desc}
 
 
 def run_reference(args, rank, world):
@@ -492,7 +652,7 @@ def run_reference(args, rank, world):
     budget = max(0.2, min(20.0, 150.0 / max(total, 1)))
     tot_tok, tot_s = 0, 0.0
     for i in range(total):
-        cb = cpu_baseline(sc, step, None, q, k, v, torch, dev, budget_s=budget)
+        cb = cpu_baseline(sc, step, None, q, k, v, torch, dev, budget_s=budget, full=False)
         if i >= args.warmup:
             tot_tok += cb["value"] * cb["seconds"]
             tot_s += cb["seconds"]
@@ -515,10 +675,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixed_2048",
-                    choices=["mixed_2048", "decode_64", "long_prompt_32k"])
+                    choices=["mixed_2048", "decode_64", "long_prompt_32k", "prefill_chunk_16k"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the decode-only and long-prompt sub-measurements")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -9,23 +9,30 @@
 // stalls), and both Q.K^T and P.V are dense contractions, so they run on the
 // tensor cores.
 //
-// One CTA = (prefill row r, KV head g, M tile of 128 query rows).  The 128
-// rows pack 128/G tokens x the G query heads that share KV head g, so each
-// K/V byte feeds G heads.  Keys stream in tiles of 128 (eight 16-token
-// pages), gathered through the block table by TMA: every page is two 2-D
-// tensor-map loads (dims 0-63 and 64-127, 128-byte swizzle) straight into the
-// canonical UMMA layout.
+// One CTA = (prefill row r, KV head g, a PAIR of 128-row query tiles).  A
+// query tile packs 128/G tokens x the G query heads that share KV head g, so
+// each K/V byte feeds G heads, and both tiles of the pair share every K/V
+// tile staged in shared memory.  Keys stream in tiles of 128 (eight 16-token
+// pages), gathered through the block table by TMA: each page is two 2-D
+// tensor-map loads (dims 0-63 and 64-127, 128-byte swizzle) that land in the
+// canonical UMMA layout; one warp instruction issues a tile's 32 loads.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread i owns query row i = TMEM lane i.  Loads Q
-//              into shared memory, reads S rows from TMEM, masks, runs the
-//              online softmax in base 2 (rescaling O in TMEM only when the
-//              running max grows by more than 2^8), writes P (bf16) to shared
-//              memory, and finally normalises O and stores it.
-//   warp 4     TMA producer: K/V tiles into a 2-stage ring (mbarrier tx).
-//   warp 5     MMA issuer: allocates 512 TMEM columns, issues
-//              S[b] = Q K^T (S double-buffered, so Q K^T of tile j+1 runs
-//              while tile j is in softmax) and O += P V, commits to mbarriers.
+// Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
+// softmax of tile t overwrites the first 64 columns of S_t with P_t as bf16
+// pairs, and P_t.V reads its A operand straight from tensor memory, so P never
+// touches shared memory.
+//
+// Warp roles (320 threads):
+//   warps 0-3 / 4-7  softmax for query tile 0 / 1: thread i owns row i (TMEM
+//              lane i).  Loads its Q row into shared memory; per KV tile reads
+//              its S row, masks, runs the online softmax in base 2 (O_t is
+//              rescaled in tensor memory only when the running max grows by
+//              more than 2^8), writes P_t back to tensor memory; at the end
+//              normalises O_t and stores it.
+//   warp 8     TMA producer: K/V tiles into a 2-stage ring.
+//   warp 9     MMA issuer: allocates tensor memory and issues, per KV tile j,
+//              P0.V(j-1), Q0.K(j), P1.V(j-1), Q1.K(j) -- so each softmax
+//              warpgroup works while the tensor core serves the other.
 // Every wait is bounded (CB_DEVERR_TIMEOUT) and nothing spins forever.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -41,33 +48,33 @@
 namespace cb {
 namespace prefill {
 
-constexpr int kBM = 128;            // query rows per CTA
+constexpr int kBM = 128;            // query rows per tile
 constexpr int kBN = 128;            // keys per KV tile
 constexpr int kD = 128;             // head dim
 constexpr int kPage = 16;           // tokens per block
 constexpr int kStages = 2;          // K/V tile ring
-constexpr int kThreads = 192;
-constexpr uint32_t kTileBytes = kBN * kD * 2;       // 32 KB (one K or V tile)
+constexpr int kThreads = 320;
+constexpr uint32_t kTileBytes = kBN * kD * 2;       // 32 KB (one Q, K or V tile)
 constexpr uint32_t kHalf = kTileBytes / 2;          // dims 0-63 | dims 64-127
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// tensor-memory column of S_t and O_t for query tile t
+__host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return t ? 384u : 256u; }
 
 struct SmemLayout {
-  static constexpr uint32_t q = 0;
-  static constexpr uint32_t k = q + kTileBytes;
+  static constexpr uint32_t q = 0;                              // Q0 | Q1
+  static constexpr uint32_t k = q + 2 * kTileBytes;
   static constexpr uint32_t v = k + kStages * kTileBytes;
-  static constexpr uint32_t p = v + kStages * kTileBytes;
-  static constexpr uint32_t bars = p + kTileBytes;
+  static constexpr uint32_t bars = v + kStages * kTileBytes;
   static constexpr uint32_t total = bars + 256;
 };
 
 struct Bars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t s_empty[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  uint64_t s_full[2];     // per query tile: S_t of the current KV tile ready
+  uint64_t p_full[2];     // per query tile: P_t written (and O_t rescaled)
+  uint64_t o_done[2];     // per query tile: last P_t.V complete
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
@@ -85,11 +92,23 @@ struct Params {
   uint32_t* error_word;
 };
 
+__device__ __forceinline__ void abort_cta(Bars* B, uint32_t* error_word) {
+  if (atomicExch(&B->abort, 1u) == 0u) set_error(error_word, CB_DEVERR_TIMEOUT);
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* B,
                                               uint32_t* error_word) {
   if (mbar_wait(bar, parity)) return true;
-  if (atomicExch(&B->abort, 1u) == 0u) set_error(error_word, CB_DEVERR_TIMEOUT);
+  abort_cta(B, error_word);
   return false;
+}
+
+// 2^x with the hardware approximation (ex2.approx.ftz.f32): relative error
+// about 2^-22, 2^-inf = 0; used for softmax weights that are rounded to bf16.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
@@ -109,10 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   const int G = p.group;
-  const int tpt = kBM / G;                       // tokens per M tile
+  const int tpt = kBM / G;                       // tokens per query tile
   const int r = p.row_begin + blockIdx.z;
   const int g = blockIdx.y;
-  const int mt = gridDim.x - 1 - blockIdx.x;     // heavy (late) tiles first
+  const int mp = gridDim.x - 1 - blockIdx.x;     // tile pair; heavy (late) pairs first
   const int q0 = p.cu_seqlens_q[r];
   const int q_len = p.cu_seqlens_q[r + 1] - q0;
   const int L = p.seq_lens[r];
@@ -122,9 +141,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
     return;
   }
-  if (mt * tpt >= q_len) return;  // this M tile is past the chunk
+  const int tok0 = mp * 2 * tpt;                 // first token of query tile 0
+  if (tok0 >= q_len) return;                     // this pair is past the chunk
+  const bool has_t1 = tok0 + tpt < q_len;        // query tile 1 holds tokens
   const int start = L - q_len;
-  const int last_tok = min(mt * tpt + tpt - 1, q_len - 1);
+  const int last_tok = min(tok0 + 2 * tpt - 1, q_len - 1);
   const int n_tiles = (start + last_tok) / kBN + 1;
   const int npages = (L + kPage - 1) / kPage;
 
@@ -133,17 +154,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&B->kv_full[s], 1);
       mbar_init(&B->kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&B->s_full[b], 1);
-      mbar_init(&B->s_empty[b], 4);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&B->s_full[t], 1);
+      mbar_init(&B->p_full[t], 4);
+      mbar_init(&B->o_done[t], 1);
     }
-    mbar_init(&B->p_full, 4);
-    mbar_init(&B->pv_done, 1);
     mbar_init(&B->drain, 1);
     B->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tc::tmem_alloc(&B->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -152,50 +172,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = B->tmem_base;
 
-  const uint32_t sQ = smem_addr(smem + SmemLayout::q);
-  const uint32_t sK = smem_addr(smem + SmemLayout::k);
-  const uint32_t sV = smem_addr(smem + SmemLayout::v);
-  const uint32_t sP = smem_addr(smem + SmemLayout::p);
-
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
+    // Lane l moves one 16-row x 64-dim box: page l/4 of the tile, part l%4
+    // (K dims 0-63, K dims 64-127, V dims 0-63, V dims 64-127), so one warp
+    // instruction issues all 32 loads of a tile.  Block ids of the next tile
+    // are fetched while waiting for a free stage.
     const int oob_row = p.num_blocks * p.num_kv_heads * kPage;  // reads as zeros
+    const int part = lane & 3;
+    const int pg = lane >> 2;
+    const CUtensorMap* tmap = part < 2 ? &tmap_k : &tmap_v;
+    const uint32_t dst_off = (part < 2 ? SmemLayout::k : SmemLayout::v) + (part & 1) * kHalf +
+                             pg * (kPage * 128);
+    const int x = (part & 1) * 64;
+    auto fetch_blk = [&](int j) -> int {
+      const int page = j * (kBN / kPage) + lane;
+      return (lane < kBN / kPage && j < n_tiles && page < npages)
+                 ? __ldg(p.block_tables + (int64_t)r * W + page)
+                 : -1;
+    };
+    auto to_row = [&](int blk, int j) -> int {
+      const int page = j * (kBN / kPage) + lane;
+      if (lane >= kBN / kPage || page >= npages) return oob_row;
+      if (blk < 0 || blk >= p.num_blocks) {
+        set_error(p.error_word, CB_DEVERR_BLOCK_RANGE);
+        return oob_row;
+      }
+      return (blk * p.num_kv_heads + g) * kPage;
+    };
     int issued = 0;
+    int blk_next = fetch_blk(0);
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kStages;
+      const int blk_cur = blk_next;
+      blk_next = fetch_blk(j + 1);  // in flight while we wait
       if (j >= kStages) {
-        bool ok = true;
-        if (lane == 0) ok = wait_or_abort(&B->kv_empty[s], ((j / kStages) - 1) & 1, B, p.error_word);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&B->kv_empty[s], ((j / kStages) - 1) & 1));
+        if (!ok) { abort_cta(B, p.error_word); break; }
       }
       if (*reinterpret_cast<volatile uint32_t*>(&B->abort)) break;
-      // lanes 0..7 look up the 8 pages of this tile
-      int row = oob_row;
-      if (lane < kBN / kPage) {
-        const int page = j * (kBN / kPage) + lane;
-        if (page < npages) {
-          const int blk = p.block_tables[(int64_t)r * W + page];
-          if (blk >= 0 && blk < p.num_blocks) {
-            row = (blk * p.num_kv_heads + g) * kPage;
-          } else {
-            set_error(p.error_word, CB_DEVERR_BLOCK_RANGE);
-          }
-        }
-      }
+      const int rr = __shfl_sync(0xffffffffu, to_row(blk_cur, j), pg);
       if (lane == 0) mbar_arrive_expect_tx(&B->kv_full[s], 2 * kTileBytes);
-      for (int pg = 0; pg < kBN / kPage; ++pg) {
-        const int rr = __shfl_sync(0xffffffffu, row, pg);
-        if (lane == 0) {
-          uint8_t* kd = smem + SmemLayout::k + s * kTileBytes + pg * (kPage * 128);
-          uint8_t* vd = smem + SmemLayout::v + s * kTileBytes + pg * (kPage * 128);
-          tc::tma_load_2d(kd, &tmap_k, 0, rr, &B->kv_full[s]);
-          tc::tma_load_2d(kd + kHalf, &tmap_k, 64, rr, &B->kv_full[s]);
-          tc::tma_load_2d(vd, &tmap_v, 0, rr, &B->kv_full[s]);
-          tc::tma_load_2d(vd + kHalf, &tmap_v, 64, rr, &B->kv_full[s]);
-        }
-      }
       __syncwarp();
+      tc::tma_load_2d(smem + dst_off + s * kTileBytes, tmap, x, rr, &B->kv_full[s]);
       issued = j + 1;
     }
     // drain: every issued load lands before the CTA may exit
@@ -203,58 +222,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
         mbar_wait(&B->kv_full[j % kStages], (j / kStages) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA
-    asm volatile("bar.sync 1, 160;" ::: "memory");  // Q is in shared memory
+    asm volatile("bar.sync 1, 288;" ::: "memory");  // Q0, Q1 are in shared memory
     tc::fence_after_sync();
     if (lane == 0) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBM, kBN, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kBM, kD, 1);
+      const uint32_t sQ = smem_addr(smem + SmemLayout::q);
+      const uint32_t sK = smem_addr(smem + SmemLayout::k);
+      const uint32_t sV = smem_addr(smem + SmemLayout::v);
+      const int nt = has_t1 ? 2 : 1;
       bool ok = true;
       for (int j = 0; j <= n_tiles && ok; ++j) {
-        if (j < n_tiles) {
-          const int s = j % kStages;
-          const int b = j & 1;
-          ok = wait_or_abort(&B->kv_full[s], (j / kStages) & 1, B, p.error_word);
-          if (ok && j >= 2) ok = wait_or_abort(&B->s_empty[b], ((j >> 1) - 1) & 1, B, p.error_word);
-          if (!ok) break;
-          tc::fence_after_sync();
-          const uint32_t d = tmem + (b ? kColS1 : kColS0);
+        const int s = j % kStages;
+        if (j < n_tiles) ok = wait_or_abort(&B->kv_full[s], (j / kStages) & 1, B, p.error_word);
+        for (int t = 0; t < nt && ok; ++t) {
+          if (j >= 1) {
+            // O_t += P_t(j-1) . V(j-1); P_t lives in the first 64 columns of S_t
+            const int jp = j - 1;
+            const int sp = jp % kStages;
+            ok = wait_or_abort(&B->p_full[t], jp & 1, B, p.error_word);
+            if (!ok) break;
+            tc::fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            tc::mma_f16(d, tc::smem_desc_sw128(sQ + off, 16, 1024),
-                        tc::smem_desc_sw128(sK + s * kTileBytes + off, 16, 1024), idesc_qk, kk > 0);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              tc::mma_f16_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8,
+                             tc::smem_desc_sw128(sV + sp * kTileBytes + kk * 2048, kHalf, 1024),
+                             idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+            if (t == nt - 1) tc::mma_commit(&B->kv_empty[sp]);
+            if (j == n_tiles) tc::mma_commit(&B->o_done[t]);
           }
-          tc::mma_commit(&B->s_full[b]);
-        }
-        if (j >= 1) {
-          const int jp = j - 1;
-          const int sp = jp % kStages;
-          ok = wait_or_abort(&B->p_full, jp & 1, B, p.error_word);
-          if (!ok) break;
-          tc::fence_after_sync();
+          if (j < n_tiles) {
+            // S_t = Q_t . K(j)^T (after P_t.V(j-1) in issue order)
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-            const uint32_t boff = sp * kTileBytes + kk * 2048;
-            tc::mma_f16(tmem + kColO, tc::smem_desc_sw128(sP + aoff, 16, 1024),
-                        tc::smem_desc_sw128(sV + boff, kHalf, 1024), idesc_pv,
-                        (jp > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+              tc::mma_f16(tmem + col_s(t),
+                          tc::smem_desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
+                          tc::smem_desc_sw128(sK + s * kTileBytes + off, 16, 1024), idesc_qk, kk > 0);
+            }
+            tc::mma_commit(&B->s_full[t]);
           }
-          tc::mma_commit(&B->pv_done);
-          tc::mma_commit(&B->kv_empty[sp]);
         }
       }
-      // drain: all issued MMAs complete before TMEM is released
+      // drain: all issued MMAs complete before tensor memory is released
       tc::mma_commit(&B->drain);
       mbar_wait(&B->drain, 0);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int row = threadIdx.x;  // 0..127 == TMEM lane
-    const int tok = mt * tpt + row / G;
+    const int t = warp >> 2;                     // query tile of this warpgroup
+    const int row = threadIdx.x & 127;           // == TMEM lane
+    const int tok = tok0 + t * tpt + row / G;
     const int head = g * G + row % G;
     const bool valid = tok < q_len;
     const int pos = start + (valid ? tok : q_len - 1);
@@ -262,88 +283,101 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       const uint4* src = reinterpret_cast<const uint4*>(
           p.q + ((int64_t)(q0 + (valid ? tok : q_len - 1)) * p.num_q_heads + head) * kD);
-      uint8_t* qs = smem + SmemLayout::q;
+      uint8_t* qs = smem + SmemLayout::q + t * kTileBytes;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(qs + (c >> 3) * kHalf + swz(row, c & 7)) = v;
       }
       fence_proxy_async_smem();
-      asm volatile("bar.sync 1, 160;" ::: "memory");
+      asm volatile("bar.sync 1, 288;" ::: "memory");
     }
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const bool active = t == 0 || has_t1;
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t colS = col_s(t), colO = col_o(t);
     float m_run = -INFINITY, l_run = 0.f;
     const float sl = p.scale_log2;
-    bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      bool w = true;
-      if (lane == 0) w = wait_or_abort(&B->s_full[b], (j >> 1) & 1, B, p.error_word);
-      w = __shfl_sync(0xffffffffu, w, 0);
-      if (!w) { ok = false; break; }
+    bool ok = active;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      bool w = __all_sync(0xffffffffu, mbar_wait(&B->s_full[t], j & 1));
+      if (!w) { abort_cta(B, p.error_word); ok = false; break; }
       tc::fence_after_sync();
-      float s[kBN];
-      const uint32_t sc = trow + (b ? kColS1 : kColS0);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(sc + 32 * c, s + 32 * c);
-      tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&B->s_empty[b]);
-
       const int kbase = j * kBN;
-      float mt_max = -INFINITY;
-      if (kbase + kBN - 1 > pos) {
+      // causal mask limit: key kbase+i is visible iff i <= lim
+      const int lim = pos - kbase;
+      const bool masked = lim < kBN - 1;
+      // pass 1: row max of the raw scores (64 columns at a time, 8 chains)
+      float mx[8];
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          s[i] = (kbase + i <= pos) ? s[i] * sl : -INFINITY;
-          mt_max = fmaxf(mt_max, s[i]);
-        }
-      } else {
+      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          s[i] *= sl;
-          mt_max = fmaxf(mt_max, s[i]);
+      for (int h = 0; h < 2; ++h) {
+        float s[64];
+        tc::tmem_ld32(trow + colS + 64 * h, s);
+        tc::tmem_ld32(trow + colS + 64 * h + 32, s + 32);
+        tc::tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) s[i] = (64 * h + i <= lim) ? s[i] : -INFINITY;
         }
+#pragma unroll
+        for (int i = 0; i < 64; i += 8)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], s[i + u]);
       }
+      const float mt_max =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
       const float m_new = fmaxf(m_run, mt_max);
       const bool resc = (m_new - m_run) > 8.f;  // also true on the first tile
       const float m_use = resc ? m_new : m_run;
-      const float alpha = resc ? exp2f(m_run - m_use) : 1.f;
+      const float alpha = resc ? fast_exp2(m_run - m_use) : 1.f;
       m_run = m_use;
-      float lsum = 0.f;
-      uint32_t pk[kBN / 2];
+      // pass 2: p = 2^(s*scale - m) (one FFMA + one ex2 per score), row sum in
+      // 8 chains, P as bf16 pairs written over S columns already read
+      const float nm = -m_use;
+      float ls[8];
 #pragma unroll
-      for (int i = 0; i < kBN; i += 2) {
-        const float a = exp2f(s[i] - m_use);
-        const float c = exp2f(s[i + 1] - m_use);
-        lsum += a + c;
-        pk[i / 2] = float2_to_bf16x2(a, c);
+      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float s[32];
+        tc::tmem_ld32(trow + colS + 32 * h, s);
+        tc::tmem_wait_ld();
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[i] = (32 * h + i <= lim) ? s[i] : -INFINITY;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float a = fast_exp2(fmaf(s[i], sl, nm));
+          const float c = fast_exp2(fmaf(s[i + 1], sl, nm));
+          ls[(i >> 1) & 7] += a + c;
+          pk[i / 2] = float2_to_bf16x2(a, c);
+        }
+        tc::tmem_st16(trow + colS + 16 * h, pk);
       }
+      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       l_run = l_run * alpha + lsum;
 
-      // P buffer and O are free once P.V of the previous tile completed
-      if (j > 0) {
-        if (lane == 0) w = wait_or_abort(&B->pv_done, (j - 1) & 1, B, p.error_word);
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) { ok = false; break; }
-        tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, resc)) {
+      // S_t(j) ready implies P_t.V(j-1) completed (same issuing thread, in
+      // order), so O_t is stable here and may be rescaled.
+      if (j >= 1 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tc::tmem_ld32(trow + kColO + 32 * c, o);
-            tc::tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tc::tmem_ld32(trow + colO + 32 * c, o);
+          tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tc::tmem_st32(trow + kColO + 32 * c, o);
-          }
-          tc::tmem_wait_st();
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tc::tmem_st32(trow + colO + 32 * c, o);
         }
       }
       // keys at or past seq_len in this tile's valid pages hold stale data;
-      // zero those V rows (P is 0 there, but 0 * NaN would not be)
-      if (kbase + kBN > L) {
+      // zero those V rows (P is 0 there, but 0 * NaN would not be).  Done by
+      // tile 0's warpgroup before P_0.V(j), the first reader of V(j).
+      if (t == 0 && kbase + kBN > L) {
         const int z0 = L - kbase;
         const int z1 = min(kBN, npages * kPage - kbase);
         const int kr = z0 + row;
@@ -355,24 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = make_uint4(0, 0, 0, 0);
           }
         }
+        fence_proxy_async_smem();
       }
-      // P row -> shared memory (K-major, 128-byte swizzle)
-      uint8_t* ps = smem + SmemLayout::p;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        *reinterpret_cast<uint4*>(ps + (c >> 3) * kHalf + swz(row, c & 7)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      }
-      fence_proxy_async_smem();
+      tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&B->p_full);
+      if (lane == 0) mbar_arrive(&B->p_full[t]);
     }
-    // epilogue: O / l -> bf16 rows
+    // epilogue: O_t / l -> bf16 rows
     if (ok) {
-      bool w = true;
-      if (lane == 0) w = wait_or_abort(&B->pv_done, (n_tiles - 1) & 1, B, p.error_word);
-      w = __shfl_sync(0xffffffffu, w, 0);
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&B->o_done[t], 0));
+      if (!w) abort_cta(B, p.error_word);
       if (w) {
         tc::fence_after_sync();
         const float inv = 1.f / l_run;
@@ -380,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float o[32];
-          tc::tmem_ld32(trow + kColO + 32 * c, o);
+          tc::tmem_ld32(trow + colO + 32 * c, o);
           tc::tmem_wait_ld();
           if (valid) {
 #pragma unroll
@@ -400,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 5) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 9) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------- host
@@ -482,8 +509,8 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   p.group = G;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.error_word = error_word;
-  const int tpt = kBM / G;
-  dim3 grid((a.max_q_len + tpt - 1) / tpt, a.num_kv_heads, a.num_reqs - a.num_decodes);
+  const int tpp = 2 * (kBM / G);  // tokens per CTA (a pair of query tiles)
+  dim3 grid((a.max_q_len + tpp - 1) / tpp, a.num_kv_heads, a.num_reqs - a.num_decodes);
   prefill_kernel<<<grid, kThreads, smem, stream>>>(mk, mv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(CB_ERR_CUDA, "prefill kernel launch: %s", cudaGetErrorString(e));

@@ -202,12 +202,27 @@ def trace_2000(seed: int = 0, num_requests: int = 2000,
         waiting=waiting, num_layers=4, value_scale=1.0, seed=seed)
 
 
+def prefill_chunk_16k(seed: int = 0, chunk: int = 512, offset: int = 16384,
+                      num_blocks: int = 4096) -> Scenario:
+    """One 512-token prefill chunk of a 32K prompt at absolute offset 16,384
+    (a mid-prompt step of the long-prompt interleave), 64 Q / 8 KV heads."""
+    running = [RunningRequest(req_id=0, prompt_len=32768, output_len=LONG_OUTPUT,
+                              num_cached=offset)]
+    return Scenario(
+        name="prefill_chunk_16k", num_q_heads=64, num_kv_heads=8, head_dim=128,
+        dtype="bf16", num_blocks=num_blocks, max_batch_tokens=chunk,
+        max_requests_per_batch=8, max_prefill_chunk=0, safety_margin=0.0,
+        max_blocks_per_seq=0, free_list=permuted_free_list(num_blocks, seed + 1),
+        running=running, waiting=[], value_scale=0.5, seed=seed)
+
+
 SCENARIOS = {
     "chunked_prefill_1000": chunked_prefill_1000,
     "decode_64": decode_64,
     "mixed_2048": mixed_2048,
     "long_prompt_32k": long_prompt_32k,
     "trace_2000": trace_2000,
+    "prefill_chunk_16k": prefill_chunk_16k,
 }
 
 

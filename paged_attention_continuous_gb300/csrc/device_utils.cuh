@@ -98,6 +98,21 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void* smem_dst, const void* g
       : "memory");
 }
 
+// 16-byte global -> shared copy through L2 (cp.async.cg); src_bytes 0
+// writes zeros instead of reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on `bar` once every cp.async issued so far by this thread has
+// landed (the barrier's expected count must include this arrival).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void set_error(uint32_t* word, uint32_t bits) {
   if (word) atomicOr(word, bits);
 }

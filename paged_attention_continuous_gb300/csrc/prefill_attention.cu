@@ -13,28 +13,32 @@
 // query tile packs 128/G tokens x the G query heads that share KV head g, so
 // each K/V byte feeds G heads, and both tiles of the pair share every K/V
 // tile staged in shared memory.  Keys stream in tiles of 128 (eight 16-token
-// pages), gathered through the block table by TMA: each page is two 2-D
-// tensor-map loads (dims 0-63 and 64-127, 128-byte swizzle) that land in the
-// canonical UMMA layout; one warp instruction issues a tile's 32 loads.
+// pages), gathered through the block table with 16-byte cp.async copies into
+// the 128-byte-swizzled canonical UMMA layout.
 //
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
 // softmax of tile t overwrites the first 64 columns of S_t with P_t as bf16
 // pairs, and P_t.V reads its A operand straight from tensor memory, so P never
 // touches shared memory.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3 / 4-7  softmax for query tile 0 / 1: thread i owns row i (TMEM
-//              lane i).  Loads its Q row into shared memory; per KV tile reads
-//              its S row, masks, runs the online softmax in base 2 (O_t is
-//              rescaled in tensor memory only when the running max grows by
-//              more than 2^8), writes P_t back to tensor memory; at the end
-//              normalises O_t and stores it.
-//   warp 8     TMA producer: K/V tiles into a 2-stage ring.
-//   warp 9     MMA issuer: allocates tensor memory and issues, per KV tile j,
-//              P0.V(j-1), Q0.K(j), P1.V(j-1), Q1.K(j) -- so each softmax
+//              lane i).  Loads its Q row into shared memory; per KV tile
+//              reads its S row (a max pass, then an exp pass that streams P
+//              back into tensor memory), runs the online softmax in base 2
+//              (O_t is rescaled in tensor memory only when the running max
+//              grows by more than 2^8); at the end normalises O_t and stores
+//              it.
+//   warps 8-9  producer: K and V tiles into 2-stage rings (cp.async,
+//              completion counted on the stage's mbarrier; rows past seq_len
+//              read 0).  K and V stages are released separately: K after the
+//              last Q.K^T that reads it, V after the last P.V, so loads run
+//              well ahead.
+//   warp 10    MMA issuer: allocates tensor memory and issues, per KV tile j,
+//              P0.V(j-1), Q0.K(j), P1.V(j-1), Q1.K(j) -- each softmax
 //              warpgroup works while the tensor core serves the other.
 // Every wait is bounded (CB_DEVERR_TIMEOUT) and nothing spins forever.
-#include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -52,8 +56,10 @@ constexpr int kBM = 128;            // query rows per tile
 constexpr int kBN = 128;            // keys per KV tile
 constexpr int kD = 128;             // head dim
 constexpr int kPage = 16;           // tokens per block
-constexpr int kStages = 2;          // K/V tile ring
-constexpr int kThreads = 320;
+constexpr int kStages = 2;          // K and V tile rings
+constexpr int kProducerWarps = 2;
+constexpr int kMmaWarp = 8 + kProducerWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;   // softmax x8, producer x2, MMA
 constexpr uint32_t kTileBytes = kBN * kD * 2;       // 32 KB (one Q, K or V tile)
 constexpr uint32_t kHalf = kTileBytes / 2;          // dims 0-63 | dims 64-127
 constexpr uint32_t kTmemCols = 512;
@@ -70,17 +76,21 @@ struct SmemLayout {
 };
 
 struct Bars {
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t s_full[2];     // per query tile: S_t of the current KV tile ready
-  uint64_t p_full[2];     // per query tile: P_t written (and O_t rescaled)
-  uint64_t o_done[2];     // per query tile: last P_t.V complete
+  uint64_t k_full[kStages];   // K tile landed
+  uint64_t v_full[kStages];   // V tile landed
+  uint64_t k_empty[kStages];  // last Q.K^T of the K tile done
+  uint64_t v_empty[kStages];  // last P.V of the V tile done
+  uint64_t s_full[2];         // per query tile: S_t of the current KV tile ready
+  uint64_t p_full[2];         // per query tile: P_t written (and O_t rescaled)
+  uint64_t o_done[2];         // per query tile: last P_t.V complete
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort;
 };
 
 struct Params {
+  const void* k_cache;
+  const void* v_cache;
   const __nv_bfloat16* q;
   __nv_bfloat16* out;
   const int32_t* cu_seqlens_q;
@@ -104,11 +114,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Ba
 }
 
 // 2^x with the hardware approximation (ex2.approx.ftz.f32): relative error
-// about 2^-22, 2^-inf = 0; used for softmax weights that are rounded to bf16.
+// about 2^-22, 2^-inf = 0.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x for a pair of f16 values with one hardware op (ex2.approx.f16x2).
+__device__ __forceinline__ __half2 fast_exp2_h2(__half2 x) {
+  uint32_t xi = *reinterpret_cast<uint32_t*>(&x), yi;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(yi) : "r"(xi));
+  return *reinterpret_cast<__half2*>(&yi);
 }
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
@@ -118,8 +135,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+    prefill_kernel(const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -151,8 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&B->kv_full[s], 1);
-      mbar_init(&B->kv_empty[s], 1);
+      mbar_init(&B->k_full[s], kProducerWarps * 32);
+      mbar_init(&B->v_full[s], kProducerWarps * 32);
+      mbar_init(&B->k_empty[s], 1);
+      mbar_init(&B->v_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&B->s_full[t], 1);
@@ -163,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     B->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc::tmem_alloc(&B->tmem_base, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -172,57 +190,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = B->tmem_base;
 
-  if (warp == 8) {
+  if (warp >= 8 && warp < kMmaWarp) {
     // ------------------------------------------------------------ producer
-    // Lane l moves one 16-row x 64-dim box: page l/4 of the tile, part l%4
-    // (K dims 0-63, K dims 64-127, V dims 0-63, V dims 64-127), so one warp
-    // instruction issues all 32 loads of a tile.  Block ids of the next tile
-    // are fetched while waiting for a free stage.
-    const int oob_row = p.num_blocks * p.num_kv_heads * kPage;  // reads as zeros
-    const int part = lane & 3;
-    const int pg = lane >> 2;
-    const CUtensorMap* tmap = part < 2 ? &tmap_k : &tmap_v;
-    const uint32_t dst_off = (part < 2 ? SmemLayout::k : SmemLayout::v) + (part & 1) * kHalf +
-                             pg * (kPage * 128);
-    const int x = (part & 1) * 64;
-    auto fetch_blk = [&](int j) -> int {
-      const int page = j * (kBN / kPage) + lane;
-      return (lane < kBN / kPage && j < n_tiles && page < npages)
-                 ? __ldg(p.block_tables + (int64_t)r * W + page)
-                 : -1;
+    // kProducerWarps warps gather each K and V tile with 16-byte cp.async
+    // copies into the 128-byte-swizzled canonical layout: thread u moves
+    // 16-byte column u%16 of rows u/16, u/16 + 4, ... of every page.  Rows at
+    // or past seq_len and pages outside the table are zero-filled by the copy
+    // itself.  Lane pg (0..7) holds the block id of page pg of the tile; the
+    // next tile's ids are fetched while waiting for a free stage.  (A TMA
+    // tensor copy of a 2 KB page half issues only every ~60-85 cycles, too
+    // slow to feed the tensor core from scattered 16-token pages.)
+    constexpr int kPT = kProducerWarps * 32;
+    const int u = threadIdx.x - 8 * 32;
+    const int c16 = u & 15;                       // 16-byte column of the row
+    const int rsub = u >> 4;                      // row within a step
+    const uint8_t* kc = reinterpret_cast<const uint8_t*>(p.k_cache);
+    const uint8_t* vc = reinterpret_cast<const uint8_t*>(p.v_cache);
+    const uint32_t sK = smem_addr(smem + SmemLayout::k);
+    const uint32_t sV = smem_addr(smem + SmemLayout::v);
+    const uint32_t col_off = (c16 >> 3) * kHalf;  // dims 0-63 | 64-127 region
+    auto fetch_blk = [&](int j, int pg) -> int {
+      const int page = j * (kBN / kPage) + pg;
+      return (j < n_tiles && page < npages) ? __ldg(p.block_tables + (int64_t)r * W + page) : -1;
     };
-    auto to_row = [&](int blk, int j) -> int {
-      const int page = j * (kBN / kPage) + lane;
-      if (lane >= kBN / kPage || page >= npages) return oob_row;
-      if (blk < 0 || blk >= p.num_blocks) {
-        set_error(p.error_word, CB_DEVERR_BLOCK_RANGE);
-        return oob_row;
-      }
-      return (blk * p.num_kv_heads + g) * kPage;
-    };
-    int issued = 0;
-    int blk_next = fetch_blk(0);
+    int blk_next[kBN / kPage];
+#pragma unroll
+    for (int pg = 0; pg < kBN / kPage; ++pg) blk_next[pg] = fetch_blk(0, pg);
+    int issued[2] = {0, 0};  // tiles whose K / V copies were issued
+    bool stop = false;
     for (int j = 0; j < n_tiles; ++j) {
       const int s = j % kStages;
-      const int blk_cur = blk_next;
-      blk_next = fetch_blk(j + 1);  // in flight while we wait
-      if (j >= kStages) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&B->kv_empty[s], ((j / kStages) - 1) & 1));
-        if (!ok) { abort_cta(B, p.error_word); break; }
+      int blk[kBN / kPage];
+#pragma unroll
+      for (int pg = 0; pg < kBN / kPage; ++pg) {
+        blk[pg] = blk_next[pg];
+        blk_next[pg] = fetch_blk(j + 1, pg);      // in flight while we wait
       }
-      if (*reinterpret_cast<volatile uint32_t*>(&B->abort)) break;
-      const int rr = __shfl_sync(0xffffffffu, to_row(blk_cur, j), pg);
-      if (lane == 0) mbar_arrive_expect_tx(&B->kv_full[s], 2 * kTileBytes);
-      __syncwarp();
-      tc::tma_load_2d(smem + dst_off + s * kTileBytes, tmap, x, rr, &B->kv_full[s]);
-      issued = j + 1;
+      // K(j) once Q.K^T of tile j-2 is done, then V(j) once P.V of tile j-2
+      // is done: K is released earlier, so it gets the longer lead
+      for (int hv = 0; hv < 2; ++hv) {
+        uint64_t* empty = hv ? &B->v_empty[s] : &B->k_empty[s];
+        uint64_t* full = hv ? &B->v_full[s] : &B->k_full[s];
+        if (j >= kStages) {
+          const bool ok = __all_sync(0xffffffffu, mbar_wait(empty, ((j / kStages) - 1) & 1));
+          if (!ok) { abort_cta(B, p.error_word); stop = true; break; }
+        }
+        if (*reinterpret_cast<volatile uint32_t*>(&B->abort)) { stop = true; break; }
+        const uint8_t* src = hv ? vc : kc;
+        const uint32_t dst = (hv ? sV : sK) + s * kTileBytes + col_off;
+#pragma unroll
+        for (int pg = 0; pg < kBN / kPage; ++pg) {
+          const int b = blk[pg];
+          const bool page_ok = b >= 0 && b < p.num_blocks;
+          if (!page_ok && b != -1 && u == 0 && hv == 0) set_error(p.error_word, CB_DEVERR_BLOCK_RANGE);
+          const int64_t page_off = page_ok ? ((int64_t)b * p.num_kv_heads + g) * (kPage * kD * 2) : 0;
+#pragma unroll
+          for (int rr = 0; rr < kPage; rr += kPT / 16) {
+            const int row = rr + rsub;                           // row within the page
+            const int key = j * kBN + pg * kPage + row;
+            const uint32_t nbytes = (page_ok && key < L) ? 16u : 0u;
+            const int64_t goff = page_ok ? page_off + row * (kD * 2) + c16 * 16 : 0;
+            cp_async16(dst + pg * (kPage * 128) + swz(row, c16 & 7), src + goff, nbytes);
+          }
+        }
+        cp_async_mbar_arrive(full);
+        issued[hv] = j + 1;
+      }
+      if (stop) break;
     }
-    // drain: every issued load lands before the CTA may exit
-    if (lane == 0) {
-      for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-        mbar_wait(&B->kv_full[j % kStages], (j / kStages) & 1);
-    }
-  } else if (warp == 9) {
+    // drain: every issued copy lands before the CTA may exit
+    for (int hv = 0; hv < 2; ++hv)
+      for (int j = (issued[hv] > kStages ? issued[hv] - kStages : 0); j < issued[hv]; ++j)
+        mbar_wait(hv ? &B->v_full[j % kStages] : &B->k_full[j % kStages], (j / kStages) & 1);
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     asm volatile("bar.sync 1, 288;" ::: "memory");  // Q0, Q1 are in shared memory
     tc::fence_after_sync();
@@ -236,7 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int j = 0; j <= n_tiles && ok; ++j) {
         const int s = j % kStages;
-        if (j < n_tiles) ok = wait_or_abort(&B->kv_full[s], (j / kStages) & 1, B, p.error_word);
+        if (j < n_tiles) ok = wait_or_abort(&B->k_full[s], (j / kStages) & 1, B, p.error_word);
+        if (ok && j >= 1)
+          ok = wait_or_abort(&B->v_full[(j - 1) % kStages], ((j - 1) / kStages) & 1, B, p.error_word);
+        // tiles are written through the generic proxy (cp.async); make them
+        // visible to the tensor core's async-proxy reads
+        fence_proxy_async_smem();
         for (int t = 0; t < nt && ok; ++t) {
           if (j >= 1) {
             // O_t += P_t(j-1) . V(j-1); P_t lives in the first 64 columns of S_t
@@ -250,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::mma_f16_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8,
                              tc::smem_desc_sw128(sV + sp * kTileBytes + kk * 2048, kHalf, 1024),
                              idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-            if (t == nt - 1) tc::mma_commit(&B->kv_empty[sp]);
+            if (t == nt - 1) tc::mma_commit(&B->v_empty[sp]);
             if (j == n_tiles) tc::mma_commit(&B->o_done[t]);
           }
           if (j < n_tiles) {
@@ -263,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           tc::smem_desc_sw128(sK + s * kTileBytes + off, 16, 1024), idesc_qk, kk > 0);
             }
             tc::mma_commit(&B->s_full[t]);
+            if (t == nt - 1) tc::mma_commit(&B->k_empty[s]);
           }
         }
       }
@@ -271,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&B->drain, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;                     // query tile of this warpgroup
     const int row = threadIdx.x & 127;           // == TMEM lane
@@ -303,34 +349,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!w) { abort_cta(B, p.error_word); ok = false; break; }
       tc::fence_after_sync();
       const int kbase = j * kBN;
-      // causal mask limit: key kbase+i is visible iff i <= lim
-      const int lim = pos - kbase;
+      const int lim = pos - kbase;               // key kbase+i visible iff i <= lim
       const bool masked = lim < kBN - 1;
-      // pass 1: row max of the raw scores (64 columns at a time, 8 chains)
+      // pass 1: row max of the raw scores (64 columns per TMEM wait)
       float mx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float s[64];
-        tc::tmem_ld32(trow + colS + 64 * h, s);
-        tc::tmem_ld32(trow + colS + 64 * h + 32, s + 32);
+      for (int hb = 0; hb < 2; ++hb) {
+        float sv[64];
+        tc::tmem_ld32(trow + colS + 64 * hb, sv);
+        tc::tmem_ld32(trow + colS + 64 * hb + 32, sv + 32);
         tc::tmem_wait_ld();
         if (masked) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) s[i] = (64 * h + i <= lim) ? s[i] : -INFINITY;
+          for (int i = 0; i < 64; ++i) sv[i] = (64 * hb + i <= lim) ? sv[i] : -INFINITY;
         }
 #pragma unroll
         for (int i = 0; i < 64; i += 8)
 #pragma unroll
-          for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], s[i + u]);
+          for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], sv[i + u]);
       }
       const float mt_max =
           fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
       const float m_new = fmaxf(m_run, mt_max);
-      const bool resc = (m_new - m_run) > 8.f;  // also true on the first tile
-      const float m_use = resc ? m_new : m_run;
+      const bool resc = (m_new - m_run) > 8.f;   // also true on the first tile
+      const float m_use = resc ? m_new : m_run;  // weights stay <= 2^8 otherwise
       const float alpha = resc ? fast_exp2(m_run - m_use) : 1.f;
       m_run = m_use;
       // pass 2: p = 2^(s*scale - m) (one FFMA + one ex2 per score), row sum in
@@ -341,18 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 8; ++u) ls[u] = 0.f;
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        float s[32];
-        tc::tmem_ld32(trow + colS + 32 * h, s);
-        tc::tmem_wait_ld();
+        float sv[32];
+        tc::tmem_ld32_sync(trow + colS + 32 * h, sv);
         if (masked) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[i] = (32 * h + i <= lim) ? s[i] : -INFINITY;
+          for (int i = 0; i < 32; ++i) sv[i] = (32 * h + i <= lim) ? sv[i] : -INFINITY;
         }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float a = fast_exp2(fmaf(s[i], sl, nm));
-          const float c = fast_exp2(fmaf(s[i + 1], sl, nm));
+          const float a = fast_exp2(fmaf(sv[i], sl, nm));
+          const float c = fast_exp2(fmaf(sv[i + 1], sl, nm));
           ls[(i >> 1) & 7] += a + c;
           pk[i / 2] = float2_to_bf16x2(a, c);
         }
@@ -360,36 +404,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       l_run = l_run * alpha + lsum;
-
       // S_t(j) ready implies P_t.V(j-1) completed (same issuing thread, in
       // order), so O_t is stable here and may be rescaled.
       if (j >= 1 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float o[32];
-          tc::tmem_ld32(trow + colO + 32 * c, o);
-          tc::tmem_wait_ld();
+          tc::tmem_ld32_sync(trow + colO + 32 * c, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
           tc::tmem_st32(trow + colO + 32 * c, o);
         }
-      }
-      // keys at or past seq_len in this tile's valid pages hold stale data;
-      // zero those V rows (P is 0 there, but 0 * NaN would not be).  Done by
-      // tile 0's warpgroup before P_0.V(j), the first reader of V(j).
-      if (t == 0 && kbase + kBN > L) {
-        const int z0 = L - kbase;
-        const int z1 = min(kBN, npages * kPage - kbase);
-        const int kr = z0 + row;
-        if (kr < z1) {
-          uint8_t* vrow = smem + SmemLayout::v + (j % kStages) * kTileBytes + kr * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vrow + kHalf + c * 16) = make_uint4(0, 0, 0, 0);
-          }
-        }
-        fence_proxy_async_smem();
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -407,8 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float o[32];
-          tc::tmem_ld32(trow + colO + 32 * c, o);
-          tc::tmem_wait_ld();
+          tc::tmem_ld32_sync(trow + colO + 32 * c, o);
           if (valid) {
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
@@ -427,45 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 9) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------- host
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// 2-D view of a cache [num_blocks * Hkv * 16 rows][128 dims] bf16; box 16
-// rows x 64 dims (128 bytes) with the 128-byte swizzle.
-cb_status make_cache_map(CUtensorMap* m, const void* base, int64_t rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
-  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return CB_OK;
-}
-
 }  // namespace prefill
 
 bool prefill_supported(int group) {
@@ -480,13 +469,6 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   if (a.head_dim != kD || a.block_size != kPage || a.dtype != CB_DTYPE_BF16) return CB_ERR_UNSUPPORTED;
   const int G = a.num_q_heads / a.num_kv_heads;
   if (!prefill_supported(G)) return CB_ERR_UNSUPPORTED;
-  const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * kPage;
-  if (rows >= (int64_t)1 << 31) return CB_ERR_UNSUPPORTED;
-  CUtensorMap mk, mv;
-  cb_status st = make_cache_map(&mk, a.k_cache, rows);
-  if (st != CB_OK) return st;
-  st = make_cache_map(&mv, a.v_cache, rows);
-  if (st != CB_OK) return st;
   const size_t smem = SmemLayout::total + 1024;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
@@ -496,6 +478,8 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   });
   if (attr != cudaSuccess) return fail(CB_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(attr));
   Params p{};
+  p.k_cache = a.k_cache;
+  p.v_cache = a.v_cache;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.cu_seqlens_q = a.cu_seqlens_q;
@@ -511,7 +495,7 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   p.error_word = error_word;
   const int tpp = 2 * (kBM / G);  // tokens per CTA (a pair of query tiles)
   dim3 grid((a.max_q_len + tpp - 1) / tpp, a.num_kv_heads, a.num_reqs - a.num_decodes);
-  prefill_kernel<<<grid, kThreads, smem, stream>>>(mk, mv, p);
+  prefill_kernel<<<grid, kThreads, smem, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(CB_ERR_CUDA, "prefill kernel launch: %s", cudaGetErrorString(e));
   return CB_OK;

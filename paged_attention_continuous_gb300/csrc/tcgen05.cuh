@@ -101,6 +101,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// Load 32 columns and wait for them.
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, float* v) {
+  tmem_ld32(taddr, v);
+  tmem_wait_ld();
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -113,6 +119,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, in
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
+}
+
+// ---- register reconfiguration (all warps of a warpgroup, converged) --------
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 // ---- descriptors -------------------------------------------------------------

@@ -43,10 +43,11 @@ import workloads  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the decode
-# kernel on this workload (profiles/decode_mixed_2048.md); None until taken
-# for the current kernel.
-DECODE_TRAFFIC_BYTES = None
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the
+# decode kernel on the mixed 2048-token step (1.72 GB read + 7.64 MB
+# written, as ncu prints them); reported only for that workload and set back
+# to None whenever the kernel changes.
+DECODE_TRAFFIC_BYTES = {"mixed_2048": 1.72e9 + 7.64e6}
 
 
 def peaks():
@@ -143,8 +144,22 @@ def append_bytes(step, Hkv, D, elem):
 
 
 # ---------------------------------------------------------- the workload
-def build_scenario(name):
-    return workloads.SCENARIOS[name]()
+def build_scenario(name, seed=0):
+    return workloads.SCENARIOS[name](seed=seed)
+
+
+def rank_scenario(name, rank):
+    """Requests are independent, so ranks shard them with no exchange: each
+    rank serves its own request set, drawn with seed = rank (weak scaling)."""
+    return build_scenario(name, seed=rank)
+
+
+def reduce_over_ranks(dist, value, op, device):
+    """One float reduced over all ranks (timing MAX, token SUM)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=op)
+    return float(t.item())
 
 
 def load_c_scheduler(cb, sc):
@@ -381,7 +396,7 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    sc = build_scenario(args.workload)
+    sc = rank_scenario(args.workload, rank)
     elem = 2 if sc.dtype == "bf16" else 4
     sched = load_c_scheduler(cb, sc)
     step = sched.schedule_step()
@@ -456,11 +471,12 @@ def run_ours(args, rank, world):
     t_dec = time_each(torch, dec_fn, K, stream) if dec_fn else 0.0
     t_pre = time_each(torch, pre_fn, K, stream) if pre_fn else 0.0
     clk = clocks.stop()
+    tokens_all = T
     if world > 1:
-        tt = torch.tensor([t_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_step = float(tt.item())
-        torch.distributed.barrier()
+        dist = torch.distributed
+        t_step = reduce_over_ranks(dist, t_step, dist.ReduceOp.MAX, dev)
+        tokens_all = int(reduce_over_ranks(dist, T, dist.ReduceOp.SUM, dev))
+        dist.barrier()
     assert ws.read_errors() == 0
 
     # ---- end to end through the public API, host buffers
@@ -486,6 +502,9 @@ def run_ours(args, rank, world):
     for i in range(e2e_steps):
         h2d_meta = e2e_step(scheds[i])
     t_e2e = time.perf_counter() - t0
+    if world > 1:
+        dist = torch.distributed
+        t_e2e = reduce_over_ranks(dist, t_e2e, dist.ReduceOp.MAX, dev)
     h2d = h2d_meta + (hq.numel() + hk.numel() + hv.numel()) * hq.element_size()
     d2h = hout.numel() * hout.element_size()
 
@@ -506,7 +525,7 @@ def run_ours(args, rank, world):
 
     line = {
         "metric": "attention tokens/s per mixed step",
-        "value": round(T * world / step_s, 1),
+        "value": round(tokens_all / step_s, 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": K,
@@ -523,7 +542,7 @@ def run_ours(args, rank, world):
                    "num_blocks": sc.num_blocks, "max_batch_tokens": sc.max_batch_tokens,
                    "l2": "inputs larger than L2 (decode KV %.2f GB per step), no flush" % (dbytes / 1e9),
                    "parallelism": f"replicas x{world}"},
-        "e2e": {"value": round(T * e2e_steps * world / t_e2e, 1), "unit": "tokens/s",
+        "e2e": {"value": round(tokens_all * e2e_steps / t_e2e, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "steps": e2e_steps,
                 "includes": "cb_schedule_step + pinned H2D of metadata and q/k/v + "
@@ -531,7 +550,7 @@ def run_ours(args, rank, world):
         "roofline": {"kernel": "decode_kernel (split-KV, bf16)", "bound": "hbm",
                      "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm, 4), "peak_source": src,
-                     "traffic": DECODE_TRAFFIC_BYTES,
+                     "traffic": DECODE_TRAFFIC_BYTES.get(sc.name),
                      "algorithmic_bytes_per_launch": dbytes,
                      "ms_per_launch": round(dec_s * 1e3, 4)},
         "prefill": {"kernel": "prefill rows", "bound": "tensor",
@@ -544,10 +563,10 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "gpu_launches": int(launches),
     }
-    if not args.no_extra:
+    if not args.no_extra and world == 1:
         line["decode_only"] = measure_decode_only(cb, torch, dev, max(K, 20), hbm)
         line["long_prompt"] = measure_long_prompt(cb, torch, dev, 3, hbm, bf16, bf16s)
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sc, step, runner, q, k, v, torch, dev,
                                             budget_s=args.cpu_seconds)
     return line
@@ -685,14 +704,17 @@ def main():
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 alone runs it; other ranks exit without work
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
     if world > 1:
         import torch
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group("nccl")
-    if args.impl == "reference":
-        line = run_reference(args, rank, world)
-    else:
-        line = run_ours(args, rank, world)
+    line = run_ours(args, rank, world)
     if rank == 0 and line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -214,7 +214,8 @@ cb_status cb_kv_append(const void* k_new, const void* v_new,
  *   out[t,h] = sum_{j<=p} softmax_j(scale * q[t,h].k[j,g]) v[j,g],
  *   g = h / (Hq/Hkv).
  * Rows [0, num_decodes) must have query length 1 and run the split-KV decode
- * kernel; the remaining rows run the prefill-chunk kernel.
+ * kernel (which also merges the splits of requests whose cache it split);
+ * the remaining rows run the prefill-chunk kernel.  Both go to `stream`.
  * ---------------------------------------------------------------------- */
 typedef struct cb_attention_args {
   const void* q;                /* device [num_tokens][Hq][D] */
@@ -250,6 +251,7 @@ typedef struct cb_attention_args {
 #define CB_DEVERR_DECODE_QLEN 0x4u  /* a decode row with query length != 1 */
 #define CB_DEVERR_SEQ_RANGE 0x8u    /* seq_len < q_len or beyond the table */
 #define CB_DEVERR_TIMEOUT 0x10u     /* a bounded wait ran out */
+#define CB_DEVERR_PLAN 0x20u        /* decode splits did not fit the partial slots */
 
 /* Workspace bytes for calls with up to num_reqs rows and these head sizes
  * (0 on bad args).  One workspace serves any later call with at most that
@@ -281,7 +283,8 @@ cb_status cb_attention_read_errors(void* workspace, size_t workspace_bytes,
  * latency-critical loop that cannot afford cudaMalloc's implicit device
  * synchronisation.  This call runs the same split-KV decode kernel as
  * cb_paged_attention but takes no workspace: its scratch (split partials,
- * tickets, work counter) lives in a fixed array of CB_NOALLOC_SCRATCH_BYTES
+ * split counters, work counters) lives in a fixed array of
+ * CB_NOALLOC_SCRATCH_BYTES
  * inside this library, which every GPU that loads the library keeps until
  * the process exits.  It allocates nothing and calls no allocating routine.
  *
@@ -292,14 +295,14 @@ cb_status cb_attention_read_errors(void* workspace, size_t workspace_bytes,
  *               (NULL: device-side errors are not reported).
  *   stream      the stream to run on.
  *
- * Limits: the scratch needed for the call, about
- * num_reqs * 32 * num_q_heads * (head_dim + 2) * 4 bytes, must fit in
- * CB_NOALLOC_SCRATCH_BYTES; larger calls are rejected with
- * CB_ERR_INVALID_ARG and a message giving the sizes.
+ * Limits: the call needs at least 2 * num_reqs * num_q_heads *
+ * (head_dim + 2) * 4 bytes of split partials in CB_NOALLOC_SCRATCH_BYTES
+ * (more room lets it cut the caches into more, smaller splits); larger
+ * calls are rejected with CB_ERR_INVALID_ARG and a message giving the sizes.
  * Set-up: the first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.
- * Every call clears the counter and tickets it needs, then uses the array;
+ * Every call clears the counters it needs, then uses the array;
  * all calls in the process share it, so calls that may overlap on the GPU
  * (different streams without ordering between them) race with each other.
  * ---------------------------------------------------------------------- */

@@ -37,6 +37,7 @@ DEVERR_SLOT_RANGE = 0x2
 DEVERR_DECODE_QLEN = 0x4
 DEVERR_SEQ_RANGE = 0x8
 DEVERR_TIMEOUT = 0x10
+DEVERR_PLAN = 0x20
 
 
 class CBError(RuntimeError):

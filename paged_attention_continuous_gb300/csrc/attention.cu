@@ -22,28 +22,32 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct WsLayout {
-  size_t header = 0, tickets = 0, prefill = 0, part_ml = 0, part_acc = 0, total = 0;
+  size_t header = 0, counters = 0, prefill = 0, part_ml = 0, part_acc = 0, total = 0;
+  int64_t slots = 0;  // decode partial slots
 };
 
-// Workspace regions.  The header, the decode tickets and the prefill region
-// hold state that must read zero at the start of every call (each call leaves
-// them zero), so they sit at FIXED offsets that do not depend on the call's
-// sizes.  The split partials are scratch rewritten by every call, sized by
-// the call's decode rows.
+// Workspace regions.  The header, the decode split counters and the prefill
+// region hold state that must read zero at the start of every call (each
+// call leaves them zero), so they sit at FIXED offsets that do not depend on
+// the call's sizes.  The split partials are scratch rewritten by every call,
+// sized by the call's decode rows.
 //   header words: [0] device error bits, [1] decode item counter,
-//                 [2] prefill item counter
+//                 [2] prefill item counter, [3] decode merge counter
+//   counters: done[kPlanMax * kMaxKvHeads], merged[kPlanMax * kMaxKvHeads]
 constexpr int64_t kMaxKvHeads = 64;
-constexpr size_t kTicketBytes = (size_t)decode::kPlanMax * kMaxKvHeads * 4;
+constexpr size_t kCounterWords = (size_t)decode::kPlanMax * kMaxKvHeads;
 
 WsLayout ws_layout(int64_t num_reqs, int64_t Hq, int64_t Hkv, int64_t D) {
   WsLayout w;
   const int64_t rows = num_reqs < decode::kPlanMax ? num_reqs : decode::kPlanMax;
   w.header = 0;
-  w.tickets = kAlign;
-  w.prefill = w.tickets + align_up(kTicketBytes);
+  w.counters = kAlign;
+  w.prefill = w.counters + align_up(2 * kCounterWords * 4);
   w.part_ml = w.prefill + align_up(prefill_workspace_bytes(Hq, Hkv, D));
-  w.part_acc = w.part_ml + align_up((size_t)rows * decode::kMaxSplits * Hq * 2 * 4);
-  w.total = w.part_acc + align_up((size_t)rows * decode::kMaxSplits * Hq * D * 4);
+  const size_t slots = (size_t)decode::partial_slots(rows, Hkv);
+  w.part_acc = w.part_ml + align_up(slots * Hq * 2 * 4);
+  w.total = w.part_acc + align_up(slots * Hq * D * 4);
+  w.slots = (int64_t)slots;
   return w;
 }
 
@@ -62,7 +66,7 @@ int sm_count() {
 template <typename T, int D, int G>
 constexpr int decode_warps() {
   using WS = decode::WarpSmem<T, D, G, 2>;
-  return sizeof(WS) * 8 + (decode::kPlanMax + 1) * 4 <= 200 * 1024 ? 8 : 4;
+  return sizeof(WS) * 8 + decode::kPlanSmemBytes <= 200 * 1024 ? 8 : 4;
 }
 
 template <typename T, int D, int G>
@@ -70,7 +74,7 @@ cb_status launch_decode(const cb_attention_args& a, const WsLayout& L, cudaStrea
   constexpr int kStages = 2;
   constexpr int kWarps = decode_warps<T, D, G>();
   using WS = decode::WarpSmem<T, D, G, kStages>;
-  const size_t smem = sizeof(WS) * kWarps + (decode::kPlanMax + 1) * 4;
+  const size_t smem = sizeof(WS) * kWarps + decode::kPlanSmemBytes;
   auto kern = decode::decode_kernel<T, D, G, kWarps, kStages>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -96,7 +100,10 @@ cb_status launch_decode(const cb_attention_args& a, const WsLayout& L, cudaStrea
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.error_word = reinterpret_cast<uint32_t*>(ws + L.header);
   p.work_counter = reinterpret_cast<uint32_t*>(ws + L.header) + 1;
-  p.tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+  p.merge_counter = reinterpret_cast<uint32_t*>(ws + L.header) + 3;
+  p.done = reinterpret_cast<uint32_t*>(ws + L.counters);
+  p.merged = p.done + kCounterWords;
+  p.max_slots = (int32_t)(L.slots < (1 << 30) ? L.slots : (1 << 30));
   p.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
   p.part_acc = reinterpret_cast<float*>(ws + L.part_acc);
   const int grid = sm_count();

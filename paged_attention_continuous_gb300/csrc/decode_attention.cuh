@@ -10,10 +10,15 @@
 // generation stalls), so this kernel is built to stream HBM:
 //
 //   * Work item = (decode row r, split s, KV head g): a run of consecutive
-//     16-token pages of one request and one KV head.  Items are handed out
-//     through a global atomic counter (dynamic load balance).  The split
-//     size is chosen in the kernel from the total page count so every warp
-//     gets several items; a request gets at most kMaxSplits splits.
+//     16-token pages of one request and one KV head.  The items come in two
+//     phases: first the leading 7/8 of every row's pages in equal large
+//     splits, dealt out statically (warp w of W takes items w, w + W, ...),
+//     then the remaining 1/8 in small splits handed out in index order
+//     through a global atomic counter, so the last items are short and the
+//     warps finish together (dynamic load balance where it matters).  Split
+//     sizes are chosen in the kernel from the total page count (a few long
+//     requests get as many splits as many short ones), and doubled until
+//     the splits fit the caller's partial slots.
 //   * Every WARP is an independent worker with its own pipeline: lane 0 issues
 //     cp.async.bulk copies (TMA engine, 1-D) of the (block, head) K page and V
 //     page -- each one contiguous block_size*D run in the cache layout
@@ -26,13 +31,17 @@
 //     butterfly reduce-scatter (warp shuffles), so each lane ends with one
 //     (token, head) score.  Online softmax in base 2 with the scale folded
 //     into q; P.V accumulates in fp32 registers (packed f32x2 FMAs).
-//   * Splits write (m, l, acc) partials; the last split of a (request, head)
-//     to finish -- an atomic ticket, no spin-wait -- merges them with the
-//     log-sum-exp rescale and writes the output.
+//   * A request with one split writes its output directly.  Otherwise every
+//     split writes an (m, l, acc) partial and counts itself done for its
+//     (request, KV head).  Warps that find no item left take merge tasks,
+//     one per (request, query head), from a second counter: wait (bounded)
+//     until the request's splits are all done -- they are all held by
+//     running warps by then -- and merge them with the log-sum-exp rescale.
 #pragma once
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <type_traits>
 
 #include "device_utils.cuh"
 
@@ -40,10 +49,24 @@ namespace cb {
 namespace decode {
 
 constexpr int kPageTokens = 16;
-constexpr int kMaxSplits = 32;
-constexpr int kMinSplitPages = 8;
-constexpr int kItemsPerWarp = 6;
-constexpr int kPlanMax = 1024;  // decode rows planned per launch
+constexpr int kTailDiv = 8;         // the last 1/kTailDiv of each row's pages: phase B
+constexpr int kMinSplitPages = 8;   // phase-A split size floor
+constexpr int kItemsA = 4;          // phase-A items per warp (target)
+constexpr int kItemsB = 4;          // phase-B items per warp (target)
+constexpr int kPlanMax = 1024;      // decode rows planned per launch
+// Partial slots a workspace provides: kSlotsPerRow per row (the splits that
+// rounding adds per row stay below this while the phase-A split is at most
+// ~20x the phase-B split, as the sizing below gives) plus the slots that
+// kMaxWorkers warps' target item counts need.  With fewer slots the kernel
+// doubles the split sizes until the plan fits (2 slots per row always do).
+constexpr int kSlotsPerRow = 32;
+constexpr int kMaxWorkers = 2048;
+__host__ __device__ constexpr int64_t partial_slots(int64_t rows, int64_t Hkv) {
+  return rows * kSlotsPerRow + ((int64_t)kMaxWorkers * (kItemsA + kItemsB) + Hkv - 1) / Hkv;
+}
+// shared memory of the plan: split-count prefixes of both phases, and each
+// row's sequence length (0 for a row that is skipped) and query token
+constexpr int kPlanSmemBytes = (2 * (kPlanMax + 1) + 2 * kPlanMax) * (int)sizeof(int32_t);
 
 struct Params {
   const void* q;
@@ -62,11 +85,32 @@ struct Params {
   int32_t num_kv_heads;
   float scale_log2;        // softmax scale * log2(e)
   uint32_t* error_word;
-  uint32_t* work_counter;
-  uint32_t* tickets;       // [num_rows * Hkv], zero between launches
+  uint32_t* work_counter;  // zero between launches (the last grab resets it)
+  uint32_t* merge_counter; // zero between launches (the last grab resets it)
+  uint32_t* done;          // [num_rows * Hkv] splits written; zero between launches
+  uint32_t* merged;        // [num_rows * Hkv] merge tasks finished; zero between launches
+  int32_t max_slots;       // partial slots available (>= 2 * num_rows)
   float* part_ml;          // [slots][Hkv][G][2]
   float* part_acc;         // [slots][Hkv][G][D]
 };
+
+// How a row of `pages` pages is cut, given the launch-wide split sizes spa
+// (phase A) and spb (phase B): phase A covers pages [0, bp) in na full
+// splits of spa pages, na = floor(leading (1 - 1/kTailDiv) of the row / spa);
+// phase B covers the rest, [bp, pages), in nb splits of spb pages (the last
+// one shorter).
+struct RowSplit {
+  int na, bp, nb;
+};
+
+__device__ __forceinline__ RowSplit row_split(int pages, int spa, int spb) {
+  RowSplit s;
+  const int big = pages - pages / kTailDiv;
+  s.na = big / spa;
+  s.bp = s.na * spa;
+  s.nb = (pages - s.bp + spb - 1) / spb;
+  return s;
+}
 
 template <typename T, int D, int G>
 struct Cfg {
@@ -144,11 +188,6 @@ __device__ __forceinline__ void store_row(T* row, int j, const float* v) {
   }
 }
 
-__device__ __forceinline__ int split_pages_for(int pages, int base_split) {
-  const int need = (pages + kMaxSplits - 1) / kMaxSplits;
-  return base_split > need ? base_split : need;
-}
-
 template <typename T, int D, int G, int kWarps, int kStages>
 __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) {
   using C = Cfg<T, D, G>;
@@ -156,9 +195,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
   constexpr int kRing = WS::kRing;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   WS* wsm_all = reinterpret_cast<WS*>(smem_raw);
-  int32_t* plan = reinterpret_cast<int32_t*>(smem_raw + sizeof(WS) * kWarps);  // [num_rows + 1]
+  int32_t* plan_a = reinterpret_cast<int32_t*>(smem_raw + sizeof(WS) * kWarps);  // [num_rows + 1]
+  int32_t* plan_b = plan_a + (kPlanMax + 1);                                        // [num_rows + 1]
+  int32_t* row_len = plan_b + (kPlanMax + 1);                                       // [num_rows]
+  int32_t* row_tok = row_len + kPlanMax;                                            // [num_rows]
   __shared__ int32_t s_red[kWarps];
-  __shared__ int32_t s_split_pages;
+  __shared__ int32_t s_red2[kWarps];
+  __shared__ int32_t s_spa, s_spb;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -167,16 +210,27 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
   const int Hq = p.num_q_heads;
   const int W = p.max_blocks_per_seq;
 
-  // ---- plan: pages per row -> split size -> prefix of split counts --------
+  // ---- plan: pages per row -> split sizes -> prefixes of split counts -----
+  // Rows are checked once here and kept in shared memory; a row that fails a
+  // check gets length 0 (no items) and its error bit.
   int64_t my_pages = 0;
   for (int i = threadIdx.x; i < p.num_rows; i += nthreads) {
     const int r = p.row_begin + i;
-    const int L = p.seq_lens[r];
+    int L = p.seq_lens[r];
+    const int q0 = p.cu_seqlens_q[r];
+    const int q1 = p.cu_seqlens_q[r + 1];
     int pages = (L + kPageTokens - 1) / kPageTokens;
     if (L < 1 || pages > W) {
-      pages = 0;
+      L = 0;
       if (blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
     }
+    if (q1 - q0 != 1 || q0 < 0 || q0 >= p.num_tokens) {
+      L = 0;
+      if (blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_DECODE_QLEN);
+    }
+    pages = (L + kPageTokens - 1) / kPageTokens;
+    row_len[i] = L;
+    row_tok[i] = q0;
     my_pages += pages;
   }
   for (int o = 16; o > 0; o >>= 1) my_pages += __shfl_xor_sync(0xffffffffu, my_pages, o);
@@ -185,50 +239,77 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
   if (threadIdx.x == 0) {
     int64_t tot = 0;
     for (int w = 0; w < kWarps; ++w) tot += s_red[w];
-    const int64_t workers = (int64_t)gridDim.x * kWarps * kItemsPerWarp;
-    int64_t sp = (tot * Hkv + workers - 1) / workers;
-    if (sp < kMinSplitPages) sp = kMinSplitPages;
-    s_split_pages = (int32_t)(sp < (1 << 20) ? sp : (1 << 20));
+    const int64_t units = tot * Hkv;
+    const int64_t units_b = units / kTailDiv;
+    const int64_t workers = (int64_t)gridDim.x * kWarps;
+    int64_t spa = (units - units_b + workers * kItemsA - 1) / (workers * kItemsA);
+    int64_t spb = (units_b + workers * kItemsB - 1) / (workers * kItemsB);
+    if (spa < kMinSplitPages) spa = kMinSplitPages;
+    if (spb < 1) spb = 1;
+    s_spa = (int32_t)(spa < (1 << 20) ? spa : (1 << 20));
+    s_spb = (int32_t)(spb < (1 << 20) ? spb : (1 << 20));
   }
   __syncthreads();
-  const int base_split = s_split_pages;
-  // serial-per-thread segments + shared scan of segment sums
-  {
+  int spa0 = s_spa, spb0 = s_spb;
+  // per row split counts of both phases and their prefixes (serial segments
+  // per thread + a block scan of the segment sums); if the splits exceed the
+  // partial slots, double both split sizes and plan again
+  for (int attempt = 0;; ++attempt) {
     const int seg = (p.num_rows + nthreads - 1) / nthreads;
     const int b = threadIdx.x * seg;
     const int e = min(b + seg, p.num_rows);
-    int sum = 0;
+    int sum_a = 0, sum_b = 0;
     for (int i = b; i < e; ++i) {
-      const int r = p.row_begin + i;
-      const int L = p.seq_lens[r];
-      int pages = (L + kPageTokens - 1) / kPageTokens;
-      int ns = 0;
-      if (L >= 1 && pages <= W) {
-        const int sp = split_pages_for(pages, base_split);
-        ns = (pages + sp - 1) / sp;
-      }
-      plan[i + 1] = ns;
-      sum += ns;
+      const RowSplit rs = row_split((row_len[i] + kPageTokens - 1) / kPageTokens, spa0, spb0);
+      const int na = rs.na, nb = rs.nb;
+      plan_a[i + 1] = na;
+      plan_b[i + 1] = nb;
+      sum_a += na;
+      sum_b += nb;
     }
-    // inclusive scan of per-thread sums
-    int incl = sum;
+    int inc_a = sum_a, inc_b = sum_b;
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      const int va = __shfl_up_sync(0xffffffffu, inc_a, o);
+      const int vb = __shfl_up_sync(0xffffffffu, inc_b, o);
+      if (lane >= o) {
+        inc_a += va;
+        inc_b += vb;
+      }
     }
-    if (lane == 31) s_red[warp] = incl;
+    if (lane == 31) {
+      s_red[warp] = inc_a;
+      s_red2[warp] = inc_b;
+    }
     __syncthreads();
-    int warp_off = 0;
-    for (int w = 0; w < warp; ++w) warp_off += s_red[w];
-    int run = warp_off + incl - sum;  // exclusive prefix of this thread's segment
-    if (threadIdx.x == 0) plan[0] = 0;
-    for (int i = b; i < e; ++i) {
-      run += plan[i + 1];
-      plan[i + 1] = run;
+    int off_a = 0, off_b = 0;
+    for (int w = 0; w < warp; ++w) {
+      off_a += s_red[w];
+      off_b += s_red2[w];
     }
+    int run_a = off_a + inc_a - sum_a, run_b = off_b + inc_b - sum_b;
+    if (threadIdx.x == 0) {
+      plan_a[0] = 0;
+      plan_b[0] = 0;
+    }
+    for (int i = b; i < e; ++i) {
+      run_a += plan_a[i + 1];
+      run_b += plan_b[i + 1];
+      plan_a[i + 1] = run_a;
+      plan_b[i + 1] = run_b;
+    }
+    __syncthreads();
+    if (plan_a[p.num_rows] + plan_b[p.num_rows] <= p.max_slots || attempt >= 40) break;
+    if (spa0 < (1 << 29)) spa0 *= 2;
+    if (spb0 < (1 << 29)) spb0 *= 2;
+    __syncthreads();  // everyone has read the totals before they are rewritten
   }
-  __syncthreads();
-  const int total_items = plan[p.num_rows] * Hkv;
+  // unreachable with max_slots >= 2 * num_rows; refuse rather than overrun
+  const bool plan_ok = plan_a[p.num_rows] + plan_b[p.num_rows] <= p.max_slots &&
+                       (int64_t)(plan_a[p.num_rows] + plan_b[p.num_rows]) * Hkv < (1 << 26);
+  if (!plan_ok && blockIdx.x == 0 && threadIdx.x == 0) set_error(p.error_word, CB_DEVERR_PLAN);
+  const int num_a = plan_a[p.num_rows];
+  const int num_b = plan_b[p.num_rows];
+  const int total_items = plan_ok ? (num_a + num_b) * Hkv : 0;
   const uint32_t total_workers = gridDim.x * kWarps;
 
   // ---- per-warp pipeline --------------------------------------------------
@@ -249,62 +330,120 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
   int prod_items = 0;      // items started by the producer
   int win_base = 0;        // first page covered by blk_win
   int blk_win = -1;        // lane i holds the block id of page win_base + i
+  int blk_win2 = -1;       // lane i: block id of page win_base + 32 + i
   bool exhausted = false;
   bool aborted = false;
   int prod_row = 0, prod_g = 0;
   uint32_t phases = 0;     // parity bit per stage
   int issued = 0, consumed = 0;
 
-  // grab the next item and describe it in the ring; false when none is left
-  auto next_item = [&]() -> bool {
-    while (true) {
-      uint32_t idx = 0;
-      if (lane == 0) idx = atomicAdd(p.work_counter, 1u);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
-      if (idx >= (uint32_t)total_items) {
-        if (idx == (uint32_t)total_items + total_workers - 1 && lane == 0) atomicExch(p.work_counter, 0u);
-        return false;
+  // Look-ahead: the item after the producer's current one is decoded, and
+  // its first block ids requested, one item early, so that the block-table
+  // load does not stall an item change.  Phase-A items come from the static
+  // deal (next_static); phase-B indices from the counter, whose next value
+  // lane 0 keeps in flight.
+  const int items_a = num_a * Hkv;
+  const uint32_t worker = blockIdx.x * kWarps + warp;
+  int next_static = (int)worker;
+  uint32_t pref_idx = 0;
+  lane0_fetch_add1(p.work_counter, pref_idx, lane);
+  // idx / Hkv without a division: floor(idx * ceil(2^32 / Hkv) / 2^32) is
+  // exact for idx < 2^26 and Hkv <= 64 (the plan keeps total_items below)
+  const uint64_t hkv_magic = (0x100000000ull + Hkv - 1) / Hkv;
+  bool nx_ok = false;
+  int nx_i = 0, nx_g = 0, nx_split = 0, nx_nsplit = 0, nx_page0 = 0, nx_page1 = 0, nx_len = 0,
+      nx_tok = 0, nx_slot = 0;
+  int nx_blk = -1;         // lane i: block id of page nx_page0 + i
+
+  // Largest row i in [0, num_rows) with plan[i] <= u (plan is a prefix sum,
+  // plan[0] = 0 <= u), i.e. the number of rows with plan[i] <= u, minus one.
+  // Warp-parallel in two levels of ballots: which of 32 segments of `step`
+  // rows holds it, then which row of that segment (num_rows <= 1024).
+  const int fr_step = (p.num_rows + 31) >> 5;
+  auto find_row = [&](const int32_t* plan, int u) -> int {
+    const int i1 = lane * fr_step;
+    const bool le1 = i1 < p.num_rows && plan[i1] <= u;
+    const int seg = __popc(__ballot_sync(0xffffffffu, le1)) - 1;
+    const int base = seg * fr_step;
+    const int i2 = base + lane;
+    const bool le2 = lane < fr_step && i2 < p.num_rows && plan[i2] <= u;
+    return base + __popc(__ballot_sync(0xffffffffu, le2)) - 1;
+  };
+
+  // decode the prefetched index into the look-ahead item and fetch the next
+  // index; nx_ok = false once the items are exhausted
+  auto fetch_ahead = [&]() {
+    nx_ok = false;
+    {
+      uint32_t idx;
+      if (next_static < items_a) {
+        idx = (uint32_t)next_static;
+        next_static += (int)total_workers;
+      } else {
+        const uint32_t b = __shfl_sync(0xffffffffu, pref_idx, 0);
+        const uint32_t items_b = (uint32_t)(total_items - items_a);
+        if (b >= items_b) {
+          if (b == items_b + total_workers - 1 && lane == 0) atomicExch(p.work_counter, 0u);
+          return;
+        }
+        lane0_fetch_add1(p.work_counter, pref_idx, lane);
+        idx = (uint32_t)items_a + b;
       }
-      // row: largest i with plan[i] * Hkv <= idx
-      int lo = 0, hi = p.num_rows - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (plan[mid] * Hkv <= (int)idx) lo = mid; else hi = mid - 1;
-      }
-      const int i = lo;
-      const int local = (int)idx - plan[i] * Hkv;
-      const int split = local / Hkv;
-      const int g = local - split * Hkv;
+      const uint32_t u = (uint32_t)(((uint64_t)idx * hkv_magic) >> 32);
+      const int g = (int)(idx - u * (uint32_t)Hkv);
+      const bool phase_a = (int)u < num_a;
+      const int i = phase_a ? find_row(plan_a, (int)u) : find_row(plan_b, (int)u - num_a);
+      const int a0 = plan_a[i], a1 = plan_a[i + 1], b0 = plan_b[i], b1 = plan_b[i + 1];
+      const int split = phase_a ? (int)u - a0 : (int)u - num_a - b0;
       const int r = p.row_begin + i;
-      const int L = p.seq_lens[r];
+      const int L = row_len[i];
       const int pages = (L + kPageTokens - 1) / kPageTokens;
-      const int sp = split_pages_for(pages, base_split);
-      const int nsplit = plan[i + 1] - plan[i];
-      const int q0 = p.cu_seqlens_q[r];
-      const int q1 = p.cu_seqlens_q[r + 1];
-      if (q1 - q0 != 1 || q0 < 0 || q0 >= p.num_tokens) {
-        if (lane == 0 && split == 0 && g == 0) set_error(p.error_word, CB_DEVERR_DECODE_QLEN);
-        continue;
+      const int na = a1 - a0;
+      const int bp = na * spa0;
+      nx_ok = true;
+      nx_i = i;
+      nx_g = g;
+      nx_split = split;
+      nx_nsplit = na + (b1 - b0);
+      if (phase_a) {
+        nx_page0 = split * spa0;
+        nx_page1 = nx_page0 + spa0;
+      } else {
+        nx_page0 = bp + split * spb0;
+        nx_page1 = min(pages, nx_page0 + spb0);
       }
-      const int slot_i = (prod_items) % kRing;
-      ++prod_items;
-      prod_slot = slot_i;
-      prod_row = r;
-      prod_g = g;
-      prod_page = split * sp;
-      prod_end = min(pages, prod_page + sp);
-      if (lane == 0) {
-        ItemDesc& d = ws.items[slot_i];
-        d.r = i; d.g = g; d.split = split; d.nsplit = nsplit;
-        d.page0 = prod_page; d.page1 = prod_end; d.seq_len = L; d.token = q0;
-        d.slot = plan[i] + split;
-      }
-      win_base = prod_page;
-      const int pg = win_base + lane;
-      blk_win = (pg < prod_end) ? p.block_tables[(int64_t)r * W + pg] : -1;
-      return true;
+      nx_len = L;
+      nx_tok = row_tok[i];
+      nx_slot = a0 + b0 + (phase_a ? split : na + split);
+      const int pg = nx_page0 + lane;
+      nx_blk = (pg < nx_page1) ? __ldg(p.block_tables + (int64_t)r * W + pg) : -1;
+      return;
     }
   };
+
+  // make the look-ahead item the producer's current one (describing it in
+  // the ring) and look one further ahead; false when none is left
+  auto next_item = [&]() -> bool {
+    if (!nx_ok) return false;
+    const int slot_i = (prod_items) % kRing;
+    ++prod_items;
+    prod_slot = slot_i;
+    prod_row = p.row_begin + nx_i;
+    prod_g = nx_g;
+    prod_page = nx_page0;
+    prod_end = nx_page1;
+    win_base = nx_page0;
+    blk_win = nx_blk;
+    if (lane == 0) {
+      ItemDesc& d = ws.items[slot_i];
+      d.r = nx_i; d.g = nx_g; d.split = nx_split; d.nsplit = nx_nsplit;
+      d.page0 = nx_page0; d.page1 = nx_page1; d.seq_len = nx_len; d.token = nx_tok;
+      d.slot = nx_slot;
+    }
+    fetch_ahead();
+    return true;
+  };
+  fetch_ahead();
 
   // refill one stage with the producer's next page (whole warp calls this)
   auto produce = [&](int st) {
@@ -314,10 +453,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
       if (!next_item()) { exhausted = true; return; }
       first = true;
     }
+    // block ids come 32 pages at a time; the next 32 are requested half way
+    // through the current window
+    if (prod_page - win_base == 16 && win_base + 32 < prod_end) {
+      const int pg = win_base + 32 + lane;
+      blk_win2 = (pg < prod_end) ? __ldg(p.block_tables + (int64_t)prod_row * W + pg) : -1;
+    }
     if (prod_page - win_base >= 32) {
-      win_base = prod_page;
-      const int pg = win_base + lane;
-      blk_win = (pg < prod_end) ? p.block_tables[(int64_t)prod_row * W + pg] : -1;
+      win_base += 32;
+      blk_win = blk_win2;
     }
     const int blk = __shfl_sync(0xffffffffu, blk_win, prod_page - win_base);
     if (lane == 0) {
@@ -329,7 +473,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
         set_error(p.error_word, CB_DEVERR_BLOCK_RANGE);
         bytes = first ? (uint32_t)C::kQBytes : 0u;
       }
-      fence_proxy_async_smem();
+      // the stage's previous contents were read (generic proxy) before the
+      // __syncwarp that precedes this call; the copies below only write it
       mbar_arrive_expect_tx(&ws.full[st], bytes);
       if (first) {
         const ItemDesc& d = ws.items[prod_slot];
@@ -356,6 +501,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
   const int tok = lane / C::kLG;
   const int j = lane - tok * C::kLG;
   const int hh = j / C::kDup;                // head whose score this lane ends with
+
+  // (row, KV head) of this warp's last partial, not yet counted done; the
+  // count follows a fence, so a merge that sees it also sees the partial
+  int pending_done = -1;
+  auto signal_pending = [&]() {
+    if (pending_done >= 0) {
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(p.done + pending_done, 1u);
+      pending_done = -1;
+    }
+  };
 
   float qf[G][C::kDPL];
   float acc[G][C::kDPL];
@@ -477,31 +634,43 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
       }
 
       // ---- P.V ------------------------------------------------------------------
+      // Slots past the sequence end hold whatever the pool held (possibly
+      // not finite), so on a partial page their V rows are zeroed before use;
+      // full pages skip the masking.
+      auto pv = [&](auto mask_tag) {
+        constexpr bool kMask = decltype(mask_tag)::value;
 #pragma unroll
-      for (int it = 0; it < C::kNIT; ++it) {
-        const int t = it * C::kTPI + tok;
-        const uint4* vrow = reinterpret_cast<const uint4*>(vp + t * C::kRowBytes);
-        float ph[G];
+        for (int it = 0; it < C::kNIT; ++it) {
+          const int t = it * C::kTPI + tok;
+          const uint4* vrow = reinterpret_cast<const uint4*>(vp + t * C::kRowBytes);
+          float ph[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) ph[h] = __shfl_sync(0xffffffffu, pr[it], tok * C::kLG + h * C::kDup);
-        const bool tv = t < valid;
+          for (int h = 0; h < G; ++h) ph[h] = __shfl_sync(0xffffffffu, pr[it], tok * C::kLG + h * C::kDup);
+          const bool tv = t < valid;
 #pragma unroll
-        for (int c = 0; c < C::kCPL; ++c) {
-          float vf[C::kEPC];
-          unpack16<T>(vrow[j + C::kLG * c], vf);
+          for (int c = 0; c < C::kCPL; ++c) {
+            float vf[C::kEPC];
+            unpack16<T>(vrow[j + C::kLG * c], vf);
+            if constexpr (kMask) {
 #pragma unroll
-          for (int e = 0; e < C::kEPC; ++e) vf[e] = tv ? vf[e] : 0.f;
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < C::kEPC; e += 2) {
-              float2 a2 = make_float2(acc[h][c * C::kEPC + e], acc[h][c * C::kEPC + e + 1]);
-              a2 = __ffma2_rn(make_float2(ph[h], ph[h]), make_float2(vf[e], vf[e + 1]), a2);
-              acc[h][c * C::kEPC + e] = a2.x;
-              acc[h][c * C::kEPC + e + 1] = a2.y;
+              for (int e = 0; e < C::kEPC; ++e) vf[e] = tv ? vf[e] : 0.f;
             }
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+              for (int e = 0; e < C::kEPC; e += 2) {
+                float2 a2 = make_float2(acc[h][c * C::kEPC + e], acc[h][c * C::kEPC + e + 1]);
+                a2 = __ffma2_rn(make_float2(ph[h], ph[h]), make_float2(vf[e], vf[e + 1]), a2);
+                acc[h][c * C::kEPC + e] = a2.x;
+                acc[h][c * C::kEPC + e + 1] = a2.y;
+              }
+          }
         }
-      }
+      };
+      if (valid == kPageTokens)
+        pv(std::false_type{});
+      else
+        pv(std::true_type{});
 
       // ---- item end -------------------------------------------------------------
       if (page + 1 == d.page1) {
@@ -513,7 +682,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
             for (int e = 0; e < C::kDPL; ++e) acc[h][e] += __shfl_xor_sync(0xffffffffu, acc[h][e], o);
           l_own += __shfl_xor_sync(0xffffffffu, l_own, o);
         }
-        const int r = p.row_begin + d.r;
         if (d.nsplit == 1) {
           T* orow = static_cast<T*>(p.out) + ((int64_t)d.token * Hq + (int64_t)d.g * G) * D;
 #pragma unroll
@@ -528,6 +696,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
             }
           }
         } else {
+          // count the previous partial of this warp done first: its stores
+          // were issued an item ago, so the fence rarely waits
+          signal_pending();
           const int64_t pslot = (int64_t)d.slot * Hkv + d.g;
           float* pacc = p.part_acc + pslot * G * D;
           float* pml = p.part_ml + pslot * G * 2;
@@ -553,48 +724,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
               }
             }
           }
-          __threadfence();
-          __syncwarp();
-          uint32_t ticket = 0;
-          if (lane == 0) ticket = atomicAdd(p.tickets + (int64_t)d.r * Hkv + d.g, 1u);
-          ticket = __shfl_sync(0xffffffffu, ticket, 0);
-          if (ticket == (uint32_t)d.nsplit - 1) {
-            // last split of (row, head): merge partials
-            __threadfence();
-            if (lane == 0) p.tickets[(int64_t)d.r * Hkv + d.g] = 0u;
-            const int64_t base = (int64_t)(d.slot - d.split) * Hkv + d.g;
-            constexpr int kVec = G * D / 4;  // float4 outputs per (row, head group)
-            T* orow = static_cast<T*>(p.out) + ((int64_t)d.token * Hq + (int64_t)d.g * G) * D;
-            for (int v4 = lane; v4 < kVec; v4 += 32) {
-              const int h = v4 / (D / 4);
-              float M = -INFINITY;
-              for (int s = 0; s < d.nsplit; ++s)
-                M = fmaxf(M, __ldcg(p.part_ml + ((base + (int64_t)s * Hkv) * G + h) * 2));
-              float L = 0.f;
-              float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-              for (int s = 0; s < d.nsplit; ++s) {
-                const int64_t ps = base + (int64_t)s * Hkv;
-                const float ms = __ldcg(p.part_ml + (ps * G + h) * 2);
-                const float ls = __ldcg(p.part_ml + (ps * G + h) * 2 + 1);
-                const float w = exp2f(ms - M);
-                L += w * ls;
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_acc + ps * G * D) + v4);
-                o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
-              }
-              const float inv = 1.f / L;
-              const int fi = v4 * 4;
-              if constexpr (sizeof(T) == 2) {
-                uint2 w2;
-                w2.x = float2_to_bf16x2(o.x * inv, o.y * inv);
-                w2.y = float2_to_bf16x2(o.z * inv, o.w * inv);
-                *reinterpret_cast<uint2*>(orow + fi) = w2;
-              } else {
-                *reinterpret_cast<float4*>(orow + fi) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-              }
-            }
-          }
+          pending_done = d.r * Hkv + d.g;  // counted at the next partial or below
         }
-        (void)r;
       }
     }
     __syncwarp();
@@ -605,6 +736,97 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
   if (aborted) {
     while (!exhausted) {
       if (!next_item()) exhausted = true;
+    }
+  }
+  signal_pending();
+
+  // ---- merge phase: one task per (decode row, query head) ----------------
+  // This warp took an index past the last item, so every split is held by a
+  // running warp and each wait below ends.  Task t merges row t / Hq, query
+  // head t % Hq: o = sum_s w_s acc_s / sum_s w_s l_s, w_s = 2^(m_s - max m),
+  // 32 splits at a time (lane k loads the k-th split's (m, l); lanes
+  // [0, D/4) each own 4 output elements).
+  const int num_tasks = plan_ok ? p.num_rows * Hq : 0;
+  constexpr int kV = D / 4;
+  static_assert(kV <= 32, "head row must fit one warp");
+  while (true) {
+    uint32_t t = 0;
+    lane0_fetch_add1(p.merge_counter, t, lane);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t >= (uint32_t)num_tasks) {
+      if (t == (uint32_t)num_tasks + total_workers - 1 && lane == 0) atomicExch(p.merge_counter, 0u);
+      break;
+    }
+    if (aborted) continue;  // only drain the counter
+    const int i = (int)t / Hq;
+    const int hq = (int)t - i * Hq;
+    const int s0 = plan_a[i] + plan_b[i];
+    const int n = plan_a[i + 1] + plan_b[i + 1] - s0;
+    if (n <= 1) continue;  // single split: written directly
+    const int q0 = row_tok[i];  // n >= 2 implies the row passed its checks
+    const int g = hq / G;
+    const int h = hq - g * G;
+    uint32_t* cnt_done = p.done + (int64_t)i * Hkv + g;
+    int ready = 1;
+    if (lane == 0) ready = wait_counter_at_least(cnt_done, (uint32_t)n) ? 1 : 0;
+    ready = __shfl_sync(0xffffffffu, ready, 0);
+    if (!ready) {
+      if (lane == 0) set_error(p.error_word, CB_DEVERR_TIMEOUT);
+      aborted = true;
+      continue;
+    }
+    __threadfence();
+    const int64_t base = (int64_t)s0 * Hkv + g;  // partial index of split 0
+    const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + base * G + h;
+    const int64_t ml_stride = (int64_t)Hkv * G;
+    const float4* pa = reinterpret_cast<const float4*>(p.part_acc) + (base * G + h) * kV + lane;
+    const int64_t acc_stride = (int64_t)Hkv * G * kV;
+    float M = -INFINITY, Ls = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int b0 = 0; b0 < n; b0 += 32) {
+      const int cnt = min(32, n - b0);
+      float2 v = make_float2(-INFINITY, 0.f);
+      if (lane < cnt) v = __ldcg(ml + (int64_t)(b0 + lane) * ml_stride);
+      float bm = v.x;
+      for (int k = 16; k > 0; k >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, k));
+      const float Mn = fmaxf(M, bm);
+      const float wl = lane < cnt ? exp2f(v.x - Mn) : 0.f;
+      float lsum = wl * v.y;
+      for (int k = 16; k > 0; k >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, k);
+      const float a_old = exp2f(M - Mn);  // 0 on the first batch
+      Ls = Ls * a_old + lsum;
+      o.x *= a_old; o.y *= a_old; o.z *= a_old; o.w *= a_old;
+      M = Mn;
+      for (int k0 = 0; k0 < cnt; k0 += 16) {
+        float4 av[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          av[u] = (k0 + u < cnt && lane < kV) ? __ldcg(pa + (int64_t)(b0 + k0 + u) * acc_stride)
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wl, k0 + u);
+          o.x += w * av[u].x; o.y += w * av[u].y; o.z += w * av[u].z; o.w += w * av[u].w;
+        }
+      }
+    }
+    if (lane < kV) {
+      const float inv = 1.f / Ls;
+      T* orow = static_cast<T*>(p.out) + ((int64_t)q0 * Hq + hq) * D + 4 * lane;
+      if constexpr (sizeof(T) == 2) {
+        uint2 w2;
+        w2.x = float2_to_bf16x2(o.x * inv, o.y * inv);
+        w2.y = float2_to_bf16x2(o.z * inv, o.w * inv);
+        *reinterpret_cast<uint2*>(orow) = w2;
+      } else {
+        *reinterpret_cast<float4*>(orow) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+      }
+    }
+    // the last of the G merges of (row, KV head) leaves its counters zero
+    __syncwarp();
+    if (lane == 0 && atomicAdd(p.merged + (int64_t)i * Hkv + g, 1u) == (uint32_t)G - 1) {
+      *cnt_done = 0u;
+      p.merged[(int64_t)i * Hkv + g] = 0u;
     }
   }
 }

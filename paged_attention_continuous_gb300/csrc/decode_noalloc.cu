@@ -9,8 +9,8 @@
 // its implicit device synchronisation, is not acceptable.  Such callers can
 // hand over their inputs and outputs but not a workspace.
 //
-// The scratch -- split partials (m, l, acc), per-(row, KV head) tickets, the
-// work counter -- lives in one file-scope __device__ array of
+// The scratch -- split partials (m, l, acc), per-(row, KV head) split
+// counters, the work counters -- lives in one file-scope __device__ array of
 // kNoAllocScratchBytes.  Every GPU that loads the library holds that array
 // until the process exits.  Host code must not use the array's name as a
 // device address (on the host it is only a stand-in); the device address is
@@ -32,18 +32,28 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_decode_scratch[kNoAllocScratchBytes];
 
 struct NoAllocLayout {
-  size_t tickets = 0, part_ml = 0, part_acc = 0, total = 0, zeroed = 0;
+  size_t counters = 0, part_ml = 0, part_acc = 0, total = 0, zeroed = 0;
+  int64_t slots = 0;  // partial slots (0: the call does not fit)
 };
 
 size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
+// As many partial slots as the decode plan would like, or as fit in the
+// array; at least 2 per row are needed (the plan then uses larger splits).
 NoAllocLayout noalloc_layout(int64_t rows, int64_t Hq, int64_t Hkv, int64_t D) {
   NoAllocLayout l;
-  l.tickets = 256;  // [0, 256): error word (unused here), work counter
-  l.part_ml = l.tickets + up256((size_t)rows * Hkv * 4);
-  l.part_acc = l.part_ml + up256((size_t)rows * decode::kMaxSplits * Hq * 2 * 4);
-  l.total = l.part_acc + up256((size_t)rows * decode::kMaxSplits * Hq * D * 4);
-  l.zeroed = l.part_ml;  // header + tickets must read zero when a launch starts
+  // [0, 256): word 1 item counter, word 3 merge counter; then done[rows *
+  // Hkv] and merged[rows * Hkv]
+  l.counters = 256;
+  l.part_ml = l.counters + up256((size_t)rows * Hkv * 2 * 4);
+  const size_t per_slot = (size_t)Hq * (D + 2) * 4;
+  const size_t room = kNoAllocScratchBytes - l.part_ml - 512;  // two roundings to 256
+  int64_t slots = decode::partial_slots(rows, Hkv);
+  if ((size_t)slots > room / per_slot) slots = (int64_t)(room / per_slot);
+  l.slots = slots >= 2 * rows ? slots : 0;
+  l.part_acc = l.part_ml + up256((size_t)slots * Hq * 2 * 4);
+  l.total = l.part_acc + up256((size_t)slots * Hq * D * 4);
+  l.zeroed = l.part_ml;  // counters must read zero when a launch starts
   return l;
 }
 
@@ -73,8 +83,8 @@ cb_status launch(const cb_attention_args& a, uint8_t* scratch, const NoAllocLayo
                  uint32_t* error_word, cudaStream_t stream) {
   constexpr int kStages = 2;
   using WS8 = decode::WarpSmem<T, D, G, kStages>;
-  constexpr int kWarps = sizeof(WS8) * 8 + (decode::kPlanMax + 1) * 4 <= 200 * 1024 ? 8 : 4;
-  const size_t smem = sizeof(WS8) * kWarps + (decode::kPlanMax + 1) * 4;
+  constexpr int kWarps = sizeof(WS8) * 8 + decode::kPlanSmemBytes <= 200 * 1024 ? 8 : 4;
+  const size_t smem = sizeof(WS8) * kWarps + decode::kPlanSmemBytes;
   auto kern = decode::decode_kernel<T, D, G, kWarps, kStages>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return fail(CB_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
@@ -99,7 +109,10 @@ cb_status launch(const cb_attention_args& a, uint8_t* scratch, const NoAllocLayo
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.error_word = error_word;
   p.work_counter = reinterpret_cast<uint32_t*>(scratch) + 1;
-  p.tickets = reinterpret_cast<uint32_t*>(scratch + L.tickets);
+  p.merge_counter = reinterpret_cast<uint32_t*>(scratch) + 3;
+  p.done = reinterpret_cast<uint32_t*>(scratch + L.counters);
+  p.merged = p.done + (size_t)a.num_decodes * a.num_kv_heads;
+  p.max_slots = (int32_t)L.slots;
   p.part_ml = reinterpret_cast<float*>(scratch + L.part_ml);
   p.part_acc = reinterpret_cast<float*>(scratch + L.part_acc);
   kern<<<sms > 0 ? sms : 152, kWarps * 32, smem, stream>>>(p);
@@ -147,16 +160,18 @@ extern "C" cb_status cb_paged_decode_noalloc(const cb_attention_args* args, uint
     return fail(CB_ERR_INVALID_ARG, "no-alloc decode: at most %d rows per call", cb::decode::kPlanMax);
   const cb::NoAllocLayout L =
       cb::noalloc_layout(a.num_reqs, a.num_q_heads, a.num_kv_heads, a.head_dim);
-  if (L.total > cb::kNoAllocScratchBytes)
+  if (L.slots == 0 || L.total > cb::kNoAllocScratchBytes)
     return fail(CB_ERR_INVALID_ARG,
-                "no-alloc decode: %d rows x %d query heads x head_dim %d need %zu scratch bytes, "
-                "more than the fixed %zu",
-                a.num_reqs, a.num_q_heads, a.head_dim, L.total, cb::kNoAllocScratchBytes);
+                "no-alloc decode: %d rows x %d query heads x head_dim %d need at least %zu "
+                "scratch bytes, more than the fixed %zu",
+                a.num_reqs, a.num_q_heads, a.head_dim,
+                (size_t)2 * a.num_reqs * a.num_q_heads * (a.head_dim + 2) * 4 + L.part_ml,
+                cb::kNoAllocScratchBytes);
   uint8_t* scratch = nullptr;
   cb_status st = cb::scratch_for_current_device(&scratch);
   if (st != CB_OK) return st;
-  // the array keeps the previous call's contents: the counter and tickets
-  // must read zero when the kernel starts
+  // the array keeps the previous call's contents: the counters must read
+  // zero when the kernel starts
   cudaError_t e = cudaMemsetAsync(scratch, 0, L.zeroed, stream);
   if (e != cudaSuccess) return fail(CB_ERR_CUDA, "clearing scratch: %s", cudaGetErrorString(e));
   return a.dtype == CB_DTYPE_BF16 ? cb::dispatch<__nv_bfloat16>(a, scratch, L, error_word, stream)

@@ -113,6 +113,36 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// atomicAdd(counter, 1) executed by lane 0 only, as one predicated
+// instruction (no branch around it, so the warp does not wait for the
+// result until it reads `value`); other lanes keep `value` unchanged.
+__device__ __forceinline__ void lane0_fetch_add1(uint32_t* counter, uint32_t& value, int lane) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.eq.s32 p, %2, 0;\n\t"
+      "@p atom.global.add.u32 %0, [%1], 1;\n\t}"
+      : "+r"(value)
+      : "l"(counter), "r"(lane)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until *counter >= target (acquire); false after kWaitTimeoutNs.
+__device__ __forceinline__ bool wait_counter_at_least(const uint32_t* counter, uint32_t target) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(100);
+    if (ld_acquire_gpu(counter) >= target) return true;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
 __device__ __forceinline__ void set_error(uint32_t* word, uint32_t bits) {
   if (word) atomicOr(word, bits);
 }

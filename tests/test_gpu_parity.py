@@ -104,6 +104,18 @@ def test_decode_many_splits_and_rows():
     _check(g[0], r[0], "bf16", "decode 70 rows")
 
 
+@pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 32, 8, 128), ("bf16", 64, 8, 128),
+                                            ("f32", 16, 4, 128)])
+def test_decode_few_long_rows(dtype, Hq, Hkv, D):
+    """A handful of very long caches next to tiny ones: each long row is cut
+    into hundreds of splits (both phases), merged by the combine kernel."""
+    sc = _decode_scenario([40001, 32768, 17, 2], Hq, Hkv, D, dtype)
+    run = ParityRun(sc)
+    st, g, r, _ = run.step()
+    assert st == 0
+    _check(g[0], r[0], dtype, "decode few long rows")
+
+
 def test_paging_invisible_on_gpu():
     """Different physical placements of the same logical cache give
     bit-identical GPU outputs."""

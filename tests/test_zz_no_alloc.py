@@ -44,15 +44,16 @@ def _args(cb, q, out, kc, vc, cu, sl, bt, max_seq_len):
 
 def test_rejects_sizes_beyond_the_fixed_scratch():
     cb, lib = _lib()
+    # 1024 rows x 64 query heads x (128 + 2) floats x 2 slots per row > 64 MiB
     a = cb.cb_attention_args(q=16, out=16, k_cache=16, v_cache=16, cu_seqlens_q=16,
-                             seq_lens=16, block_tables=16, num_reqs=1000, num_decodes=1000,
-                             num_tokens=1000, max_q_len=1, max_seq_len=16, num_blocks=10,
+                             seq_lens=16, block_tables=16, num_reqs=1024, num_decodes=1024,
+                             num_tokens=1024, max_q_len=1, max_seq_len=16, num_blocks=10,
                              max_blocks_per_seq=4, block_size=16, num_q_heads=64,
                              num_kv_heads=8, head_dim=128, scale=0.1, dtype=cb.DTYPE_BF16)
     st = lib.cb_paged_decode_noalloc(ctypes.byref(a), None, None)
     assert st == cb.CB_ERR_INVALID_ARG
     assert "scratch" in lib.cb_last_error().decode()
-    a.num_decodes = 999   # a prefill row present: refused, it serves decodes only
+    a.num_decodes = 1023  # a prefill row present: refused, it serves decodes only
     assert lib.cb_paged_decode_noalloc(ctypes.byref(a), None, None) == cb.CB_ERR_INVALID_ARG
 
 
@@ -94,3 +95,42 @@ def test_no_alloc_decode_matches_workspace_entry_point_twice():
         rf = ref.double().cpu().numpy()
         assert np.isfinite(g).all()
         assert (np.abs(g - rf) <= BF16_ATOL + BF16_RTOL * np.abs(rf)).all(), f"call {call}"
+
+
+@pytest.mark.gpu
+def test_no_alloc_many_rows_plans_larger_splits():
+    """800 rows x 64 query heads leave the fixed scratch room for fewer
+    partial slots than the plan first asks for; the kernel then plans larger
+    splits and must still agree with the workspace entry point."""
+    cb, lib = _lib()
+    dev = "cuda"
+    Hq, Hkv, D, bs, R = 64, 8, 128, 16, 800
+    rng = np.random.default_rng(5)
+    nb = 3000
+    kc = workloads.cache_fill(nb, Hkv, bs, D, seed=51, dtype="bf16", scale=0.5, device=dev)
+    vc = workloads.cache_fill(nb, Hkv, bs, D, seed=52, dtype="bf16", scale=0.5, device=dev)
+    seq = rng.integers(2, 600, size=R).astype(np.int32)
+    W = int(-(-seq.max() // bs))
+    bt = np.full((R, W), -1, dtype=np.int32)
+    for r in range(R):
+        n = int(-(-seq[r] // bs))
+        bt[r, :n] = rng.choice(nb, size=n, replace=False)  # rows may share blocks
+    cu = torch.arange(R + 1, dtype=torch.int32, device=dev)
+    sl = torch.from_numpy(seq).to(dev)
+    btd = torch.from_numpy(bt).to(dev)
+    q = workloads.token_tensors(R, Hq, D, seed=60, dtype="bf16", scale=0.5, device=dev)
+    ref = cb.paged_attention(q, kc, vc, cu, sl, btd, num_decodes=R, max_q_len=1,
+                             max_seq_len=int(seq.max()), scale=D ** -0.5,
+                             workspace=cb.Workspace(R, Hq, Hkv, D))
+    out = torch.full_like(q, float("nan"))
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    a = _args(cb, q, out, kc, vc, cu, sl, btd, int(seq.max()))
+    st = lib.cb_paged_decode_noalloc(ctypes.byref(a), err.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream)
+    assert st == cb.CB_OK, lib.cb_last_error().decode()
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    g = out.double().cpu().numpy()
+    rf = ref.double().cpu().numpy()
+    assert np.isfinite(g).all()
+    assert (np.abs(g - rf) <= BF16_ATOL + BF16_RTOL * np.abs(rf)).all()

@@ -273,39 +273,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sK = smem_addr(smem + SmemLayout::k);
       const uint32_t sV = smem_addr(smem + SmemLayout::v);
       const int nt = has_t1 ? 2 : 1;
+      // Shared-memory descriptors of the tiles' first k-step; a k-step's
+      // descriptor is the base plus its byte offset >> 4 (the start-address
+      // field is the low 14 bits and the tiles lie below 256 KB).
+      uint64_t dq[2], dk[kStages], dv[kStages];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) dq[t] = tc::smem_desc_sw128(sQ + t * kTileBytes, 16, 1024);
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) {
+        dk[s] = tc::smem_desc_sw128(sK + s * kTileBytes, 16, 1024);
+        dv[s] = tc::smem_desc_sw128(sV + s * kTileBytes, kHalf, 1024);
+      }
+      // Per KV tile j: P0.V(j-1), Q0.K(j), P1.V(j-1), Q1.K(j).  Each op waits
+      // only for its own inputs (P.V: the softmax's P and V(j-1); Q.K: K(j)),
+      // so a late K tile does not hold back the P.V before it.  S_t is free
+      // for Q_t.K(j) because P_t.V(j-1) was issued before it.
       bool ok = true;
       for (int j = 0; j <= n_tiles && ok; ++j) {
         const int s = j % kStages;
-        if (j < n_tiles) ok = wait_or_abort(&B->k_full[s], (j / kStages) & 1, B, p.error_word);
-        if (ok && j >= 1)
-          ok = wait_or_abort(&B->v_full[(j - 1) % kStages], ((j - 1) / kStages) & 1, B, p.error_word);
-        // tiles are written through the generic proxy (cp.async); make them
-        // visible to the tensor core's async-proxy reads
-        fence_proxy_async_smem();
         for (int t = 0; t < nt && ok; ++t) {
           if (j >= 1) {
-            // O_t += P_t(j-1) . V(j-1); P_t lives in the first 64 columns of S_t
             const int jp = j - 1;
             const int sp = jp % kStages;
             ok = wait_or_abort(&B->p_full[t], jp & 1, B, p.error_word);
+            if (ok && t == 0) ok = wait_or_abort(&B->v_full[sp], (jp / kStages) & 1, B, p.error_word);
             if (!ok) break;
+            // V was written through the generic proxy (cp.async); P by tcgen05.st
+            fence_proxy_async_smem();
             tc::fence_after_sync();
+            const uint64_t bv = dv[sp];
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              tc::mma_f16_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8,
-                             tc::smem_desc_sw128(sV + sp * kTileBytes + kk * 2048, kHalf, 1024),
+              tc::mma_f16_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, bv + (kk * 2048 >> 4),
                              idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
             if (t == nt - 1) tc::mma_commit(&B->v_empty[sp]);
             if (j == n_tiles) tc::mma_commit(&B->o_done[t]);
           }
           if (j < n_tiles) {
-            // S_t = Q_t . K(j)^T (after P_t.V(j-1) in issue order)
+            if (t == 0) {
+              ok = wait_or_abort(&B->k_full[s], (j / kStages) & 1, B, p.error_word);
+              if (!ok) break;
+              fence_proxy_async_smem();
+            }
+            const uint64_t aq = t ? dq[1] : dq[0];
+            const uint64_t bk = dk[s];
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-              tc::mma_f16(tmem + col_s(t),
-                          tc::smem_desc_sw128(sQ + t * kTileBytes + off, 16, 1024),
-                          tc::smem_desc_sw128(sK + s * kTileBytes + off, 16, 1024), idesc_qk, kk > 0);
+              const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+              tc::mma_f16(tmem + col_s(t), aq + off, bk + off, idesc_qk, kk > 0);
             }
             tc::mma_commit(&B->s_full[t]);
             if (t == nt - 1) tc::mma_commit(&B->k_empty[s]);
@@ -351,25 +366,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kbase = j * kBN;
       const int lim = pos - kbase;               // key kbase+i visible iff i <= lim
       const bool masked = lim < kBN - 1;
-      // pass 1: row max of the raw scores (64 columns per TMEM wait)
+      // the whole S row in registers with one TMEM wait
+      float sv[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) tc::tmem_ld32(trow + colS + 32 * c, sv + 32 * c);
+      tc::tmem_wait_ld();
+      if (masked) {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
+      }
       float mx[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = -INFINITY;
+      for (int u = 0; u < 8; ++u) mx[u] = sv[u];
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        float sv[64];
-        tc::tmem_ld32(trow + colS + 64 * hb, sv);
-        tc::tmem_ld32(trow + colS + 64 * hb + 32, sv + 32);
-        tc::tmem_wait_ld();
-        if (masked) {
+      for (int i = 8; i < kBN; i += 8)
 #pragma unroll
-          for (int i = 0; i < 64; ++i) sv[i] = (64 * hb + i <= lim) ? sv[i] : -INFINITY;
-        }
-#pragma unroll
-        for (int i = 0; i < 64; i += 8)
-#pragma unroll
-          for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], sv[i + u]);
-      }
+        for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], sv[i + u]);
       const float mt_max =
           fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
@@ -378,25 +390,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_use = resc ? m_new : m_run;  // weights stay <= 2^8 otherwise
       const float alpha = resc ? fast_exp2(m_run - m_use) : 1.f;
       m_run = m_use;
-      // pass 2: p = 2^(s*scale - m) (one FFMA + one ex2 per score), row sum in
-      // 8 chains, P as bf16 pairs written over S columns already read
+      // p = 2^(s*scale - m) (one FFMA + one ex2 per score), row sum in 8
+      // chains, P as bf16 pairs written over the S columns (all read above)
       const float nm = -m_use;
       float ls[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) ls[u] = 0.f;
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        float sv[32];
-        tc::tmem_ld32_sync(trow + colS + 32 * h, sv);
-        if (masked) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[i] = (32 * h + i <= lim) ? sv[i] : -INFINITY;
-        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float a = fast_exp2(fmaf(sv[i], sl, nm));
-          const float c = fast_exp2(fmaf(sv[i + 1], sl, nm));
+          const float a = fast_exp2(fmaf(sv[32 * h + i], sl, nm));
+          const float c = fast_exp2(fmaf(sv[32 * h + i + 1], sl, nm));
           ls[(i >> 1) & 7] += a + c;
           pk[i / 2] = float2_to_bf16x2(a, c);
         }

@@ -13,15 +13,16 @@
 // query tile packs 128/G tokens x the G query heads that share KV head g, so
 // each K/V byte feeds G heads, and both tiles of the pair share every K/V
 // tile staged in shared memory.  Keys stream in tiles of 128 (eight 16-token
-// pages), gathered through the block table with 16-byte cp.async copies into
-// the 128-byte-swizzled canonical UMMA layout.
+// pages), gathered through the block table by the TMA engine: one 2-D
+// tensor-map box of 16 rows x 64 dims per page half lands directly in the
+// 128-byte-swizzled canonical UMMA layout.
 //
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The
 // softmax of tile t overwrites the first 64 columns of S_t with P_t as bf16
 // pairs, and P_t.V reads its A operand straight from tensor memory, so P never
 // touches shared memory.
 //
-// Warp roles (352 threads):
+// Warp roles (384 threads):
 //   warps 0-3 / 4-7  softmax for query tile 0 / 1: thread i owns row i (TMEM
 //              lane i).  Loads its Q row into shared memory; per KV tile
 //              reads its S row (a max pass, then an exp pass that streams P
@@ -29,15 +30,20 @@
 //              (O_t is rescaled in tensor memory only when the running max
 //              grows by more than 2^8); at the end normalises O_t and stores
 //              it.
-//   warps 8-9  producer: K and V tiles into 2-stage rings (cp.async,
-//              completion counted on the stage's mbarrier; rows past seq_len
-//              read 0).  K and V stages are released separately: K after the
-//              last Q.K^T that reads it, V after the last P.V, so loads run
-//              well ahead.
-//   warp 10    MMA issuer: allocates tensor memory and issues, per KV tile j,
-//              P0.V(j-1), Q0.K(j), P1.V(j-1), Q1.K(j) -- each softmax
-//              warpgroup works while the tensor core serves the other.
+//   warp 8     K producer: K tiles into a 3-stage ring (TMA; pages past the
+//              sequence read as zeros); a stage is released after the last
+//              Q.K^T that reads it.
+//   warp 9     V producer: V tiles into a 2-stage ring, released after the
+//              last P.V.  (Slots past seq_len inside the last page are real
+//              pool memory: their K scores are masked by the softmax, their
+//              V rows are zeroed in shared memory before the P.V that reads
+//              them, as P = 0 there does not cancel a non-finite value.)
+//   warps 10-11  MMA issuers, one per query tile t (warp 10 also allocates
+//              tensor memory): per KV tile j, P_t.V(j-1) then Q_t.K(j), each
+//              as soon as its own inputs are ready -- each softmax warpgroup
+//              works while the tensor core serves the other.
 // Every wait is bounded (CB_DEVERR_TIMEOUT) and nothing spins forever.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -56,10 +62,11 @@ constexpr int kBM = 128;            // query rows per tile
 constexpr int kBN = 128;            // keys per KV tile
 constexpr int kD = 128;             // head dim
 constexpr int kPage = 16;           // tokens per block
-constexpr int kStages = 2;          // K and V tile rings
+constexpr int kStagesK = 3;         // K tile ring (K is needed first: deeper)
+constexpr int kStagesV = 2;         // V tile ring
 constexpr int kProducerWarps = 2;
-constexpr int kMmaWarp = 8 + kProducerWarps;
-constexpr int kThreads = (kMmaWarp + 1) * 32;   // softmax x8, producer x2, MMA
+constexpr int kMmaWarp = 8 + kProducerWarps;   // MMA issuers: warps kMmaWarp + t
+constexpr int kThreads = (kMmaWarp + 2) * 32;   // softmax x8, producer x2, MMA x2
 constexpr uint32_t kTileBytes = kBN * kD * 2;       // 32 KB (one Q, K or V tile)
 constexpr uint32_t kHalf = kTileBytes / 2;          // dims 0-63 | dims 64-127
 constexpr uint32_t kTmemCols = 512;
@@ -70,25 +77,27 @@ __host__ __device__ constexpr uint32_t col_o(int t) { return t ? 384u : 256u; }
 struct SmemLayout {
   static constexpr uint32_t q = 0;                              // Q0 | Q1
   static constexpr uint32_t k = q + 2 * kTileBytes;
-  static constexpr uint32_t v = k + kStages * kTileBytes;
-  static constexpr uint32_t bars = v + kStages * kTileBytes;
+  static constexpr uint32_t v = k + kStagesK * kTileBytes;
+  static constexpr uint32_t bars = v + kStagesV * kTileBytes;
   static constexpr uint32_t total = bars + 256;
 };
 
 struct Bars {
-  uint64_t k_full[kStages];   // K tile landed
-  uint64_t v_full[kStages];   // V tile landed
-  uint64_t k_empty[kStages];  // last Q.K^T of the K tile done
-  uint64_t v_empty[kStages];  // last P.V of the V tile done
+  uint64_t k_full[kStagesK];   // K tile landed
+  uint64_t v_full[kStagesV];   // V tile landed
+  uint64_t k_empty[kStagesK];  // last Q.K^T of the K tile done
+  uint64_t v_empty[kStagesV];  // last P.V of the V tile done
   uint64_t s_full[2];         // per query tile: S_t of the current KV tile ready
   uint64_t p_full[2];         // per query tile: P_t written (and O_t rescaled)
   uint64_t o_done[2];         // per query tile: last P_t.V complete
-  uint64_t drain;
+  uint64_t drain[2];          // per MMA issuer: all its MMAs complete
   uint32_t tmem_base;
   uint32_t abort;
 };
 
 struct Params {
+  CUtensorMap tmap_k;  // [num_blocks * Hkv * 16 rows][128 dims] bf16, box 16 x 64, 128-B swizzle
+  CUtensorMap tmap_v;
   const void* k_cache;
   const void* v_cache;
   const __nv_bfloat16* q;
@@ -135,7 +144,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const Params p) {
+    prefill_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -166,18 +175,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int npages = (L + kPage - 1) / kPage;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&B->k_full[s], kProducerWarps * 32);
-      mbar_init(&B->v_full[s], kProducerWarps * 32);
-      mbar_init(&B->k_empty[s], 1);
-      mbar_init(&B->v_empty[s], 1);
+    // a stage is free once every active MMA issuer (one per query tile)
+    // has committed its last read of it
+    const uint32_t issuers = has_t1 ? 2u : 1u;
+    for (int s = 0; s < kStagesK; ++s) {
+      mbar_init(&B->k_full[s], 1);
+      mbar_init(&B->k_empty[s], issuers);
+    }
+    for (int s = 0; s < kStagesV; ++s) {
+      mbar_init(&B->v_full[s], 1);
+      mbar_init(&B->v_empty[s], issuers);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&B->s_full[t], 1);
       mbar_init(&B->p_full[t], 4);
       mbar_init(&B->o_done[t], 1);
     }
-    mbar_init(&B->drain, 1);
+    mbar_init(&B->drain[0], 1);
+    mbar_init(&B->drain[1], 1);
     B->abort = 0;
     fence_barrier_init();
   }
@@ -191,145 +206,127 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = B->tmem_base;
 
   if (warp >= 8 && warp < kMmaWarp) {
-    // ------------------------------------------------------------ producer
-    // kProducerWarps warps gather each K and V tile with 16-byte cp.async
-    // copies into the 128-byte-swizzled canonical layout: thread u moves
-    // 16-byte column u%16 of rows u/16, u/16 + 4, ... of every page.  Rows at
-    // or past seq_len and pages outside the table are zero-filled by the copy
-    // itself.  Lane pg (0..7) holds the block id of page pg of the tile; the
-    // next tile's ids are fetched while waiting for a free stage.  (A TMA
-    // tensor copy of a 2 KB page half issues only every ~60-85 cycles, too
-    // slow to feed the tensor core from scattered 16-token pages.)
-    constexpr int kPT = kProducerWarps * 32;
-    const int u = threadIdx.x - 8 * 32;
-    const int c16 = u & 15;                       // 16-byte column of the row
-    const int rsub = u >> 4;                      // row within a step
-    const uint8_t* kc = reinterpret_cast<const uint8_t*>(p.k_cache);
-    const uint8_t* vc = reinterpret_cast<const uint8_t*>(p.v_cache);
-    const uint32_t sK = smem_addr(smem + SmemLayout::k);
-    const uint32_t sV = smem_addr(smem + SmemLayout::v);
-    const uint32_t col_off = (c16 >> 3) * kHalf;  // dims 0-63 | 64-127 region
-    auto fetch_blk = [&](int j, int pg) -> int {
-      const int page = j * (kBN / kPage) + pg;
-      return (j < n_tiles && page < npages) ? __ldg(p.block_tables + (int64_t)r * W + page) : -1;
+    // ------------------------------------------------------------ producers
+    // Warp 8 streams K tiles, warp 9 V tiles.  Lane pg (0..7) looks up the
+    // block of page pg of a tile (the next tile's ids are requested while the
+    // current tile waits for a free stage); lane 0 issues the two boxes of
+    // every page.  A page outside the sequence or the table uses a row past
+    // the end of the tensor map, which the TMA engine reads as zeros.
+    const int hv = warp - 8;  // 0: K, 1: V
+    const CUtensorMap* tmap = hv ? &p.tmap_v : &p.tmap_k;
+    const int nst = hv ? kStagesV : kStagesK;
+    const uint32_t ring = hv ? SmemLayout::v : SmemLayout::k;
+    const int oob_row = p.num_blocks * p.num_kv_heads * kPage;
+    auto page_row = [&](int j) -> int {
+      const int page = j * (kBN / kPage) + lane;
+      int row = oob_row;
+      if (lane < kBN / kPage && j < n_tiles && page < npages) {
+        const int blk = __ldg(p.block_tables + (int64_t)r * W + page);
+        if (blk >= 0 && blk < p.num_blocks)
+          row = (blk * p.num_kv_heads + g) * kPage;
+        else if (hv == 0)
+          set_error(p.error_word, CB_DEVERR_BLOCK_RANGE);
+      }
+      return row;
     };
-    int blk_next[kBN / kPage];
-#pragma unroll
-    for (int pg = 0; pg < kBN / kPage; ++pg) blk_next[pg] = fetch_blk(0, pg);
-    int issued[2] = {0, 0};  // tiles whose K / V copies were issued
-    bool stop = false;
+    int row_next = page_row(0);
+    int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
-      const int s = j % kStages;
-      int blk[kBN / kPage];
+      const int row = row_next;
+      row_next = page_row(j + 1);  // in flight while we wait
+      const int s = j % nst;
+      uint64_t* full = hv ? &B->v_full[s] : &B->k_full[s];
+      if (j >= nst) {
+        uint64_t* empty = hv ? &B->v_empty[s] : &B->k_empty[s];
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(empty, ((j / nst) - 1) & 1));
+        if (!ok) { abort_cta(B, p.error_word); break; }
+      }
+      if (*reinterpret_cast<volatile uint32_t*>(&B->abort)) break;
+      if (lane == 0) mbar_arrive_expect_tx(full, kTileBytes);
 #pragma unroll
       for (int pg = 0; pg < kBN / kPage; ++pg) {
-        blk[pg] = blk_next[pg];
-        blk_next[pg] = fetch_blk(j + 1, pg);      // in flight while we wait
-      }
-      // K(j) once Q.K^T of tile j-2 is done, then V(j) once P.V of tile j-2
-      // is done: K is released earlier, so it gets the longer lead
-      for (int hv = 0; hv < 2; ++hv) {
-        uint64_t* empty = hv ? &B->v_empty[s] : &B->k_empty[s];
-        uint64_t* full = hv ? &B->v_full[s] : &B->k_full[s];
-        if (j >= kStages) {
-          const bool ok = __all_sync(0xffffffffu, mbar_wait(empty, ((j / kStages) - 1) & 1));
-          if (!ok) { abort_cta(B, p.error_word); stop = true; break; }
+        const int rr = __shfl_sync(0xffffffffu, row, pg);
+        if (lane == 0) {
+          uint8_t* d = smem + ring + s * kTileBytes + pg * (kPage * 128);
+          tc::tma_load_2d(d, tmap, 0, rr, full);
+          tc::tma_load_2d(d + kHalf, tmap, 64, rr, full);
         }
-        if (*reinterpret_cast<volatile uint32_t*>(&B->abort)) { stop = true; break; }
-        const uint8_t* src = hv ? vc : kc;
-        const uint32_t dst = (hv ? sV : sK) + s * kTileBytes + col_off;
-#pragma unroll
-        for (int pg = 0; pg < kBN / kPage; ++pg) {
-          const int b = blk[pg];
-          const bool page_ok = b >= 0 && b < p.num_blocks;
-          if (!page_ok && b != -1 && u == 0 && hv == 0) set_error(p.error_word, CB_DEVERR_BLOCK_RANGE);
-          const int64_t page_off = page_ok ? ((int64_t)b * p.num_kv_heads + g) * (kPage * kD * 2) : 0;
-#pragma unroll
-          for (int rr = 0; rr < kPage; rr += kPT / 16) {
-            const int row = rr + rsub;                           // row within the page
-            const int key = j * kBN + pg * kPage + row;
-            const uint32_t nbytes = (page_ok && key < L) ? 16u : 0u;
-            const int64_t goff = page_ok ? page_off + row * (kD * 2) + c16 * 16 : 0;
-            cp_async16(dst + pg * (kPage * 128) + swz(row, c16 & 7), src + goff, nbytes);
-          }
-        }
-        cp_async_mbar_arrive(full);
-        issued[hv] = j + 1;
       }
-      if (stop) break;
+      __syncwarp();
+      issued = j + 1;
     }
     // drain: every issued copy lands before the CTA may exit
-    for (int hv = 0; hv < 2; ++hv)
-      for (int j = (issued[hv] > kStages ? issued[hv] - kStages : 0); j < issued[hv]; ++j)
-        mbar_wait(hv ? &B->v_full[j % kStages] : &B->k_full[j % kStages], (j / kStages) & 1);
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA
-    asm volatile("bar.sync 1, 288;" ::: "memory");  // Q0, Q1 are in shared memory
+    for (int j = (issued > nst ? issued - nst : 0); j < issued; ++j)
+      mbar_wait(hv ? &B->v_full[j % nst] : &B->k_full[j % nst], (j / nst) & 1);
+  } else if (warp >= kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    // Warp kMmaWarp + t issues the MMAs of query tile t: per KV tile j,
+    // P_t.V(j-1) (after the softmax wrote P_t(j-1) and V(j-1) landed), then
+    // Q_t.K(j) (after K(j) landed).  S_t is free for Q_t.K(j) because
+    // P_t.V(j-1) was issued before it.  With one issuer per tile, neither
+    // tile's chain waits behind the other's issue.
+    asm volatile("bar.sync 1, 320;" ::: "memory");  // Q0, Q1 are in shared memory
     tc::fence_after_sync();
-    if (lane == 0) {
+    const int t = warp - kMmaWarp;
+    if (lane == 0 && (t == 0 || has_t1)) {
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kBM, kBN, 0);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kBM, kD, 1);
-      const uint32_t sQ = smem_addr(smem + SmemLayout::q);
-      const uint32_t sK = smem_addr(smem + SmemLayout::k);
-      const uint32_t sV = smem_addr(smem + SmemLayout::v);
-      const int nt = has_t1 ? 2 : 1;
       // Shared-memory descriptors of the tiles' first k-step; a k-step's
       // descriptor is the base plus its byte offset >> 4 (the start-address
-      // field is the low 14 bits and the tiles lie below 256 KB).
-      uint64_t dq[2], dk[kStages], dv[kStages];
-#pragma unroll
-      for (int t = 0; t < 2; ++t) dq[t] = tc::smem_desc_sw128(sQ + t * kTileBytes, 16, 1024);
-#pragma unroll
-      for (int s = 0; s < kStages; ++s) {
-        dk[s] = tc::smem_desc_sw128(sK + s * kTileBytes, 16, 1024);
-        dv[s] = tc::smem_desc_sw128(sV + s * kTileBytes, kHalf, 1024);
-      }
-      // Per KV tile j: P0.V(j-1), Q0.K(j), P1.V(j-1), Q1.K(j).  Each op waits
-      // only for its own inputs (P.V: the softmax's P and V(j-1); Q.K: K(j)),
-      // so a late K tile does not hold back the P.V before it.  S_t is free
-      // for Q_t.K(j) because P_t.V(j-1) was issued before it.
+      // field is the low 14 bits and the tiles lie below 256 KB); stage s of
+      // a ring adds s * kTileBytes >> 4.
+      const uint64_t aq = tc::smem_desc_sw128(smem_addr(smem + SmemLayout::q) + t * kTileBytes, 16, 1024);
+      const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(smem + SmemLayout::k), 16, 1024);
+      const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(smem + SmemLayout::v), kHalf, 1024);
+      constexpr uint32_t kTileDesc = kTileBytes >> 4;
       bool ok = true;
       for (int j = 0; j <= n_tiles && ok; ++j) {
-        const int s = j % kStages;
-        for (int t = 0; t < nt && ok; ++t) {
-          if (j >= 1) {
-            const int jp = j - 1;
-            const int sp = jp % kStages;
-            ok = wait_or_abort(&B->p_full[t], jp & 1, B, p.error_word);
-            if (ok && t == 0) ok = wait_or_abort(&B->v_full[sp], (jp / kStages) & 1, B, p.error_word);
-            if (!ok) break;
-            // V was written through the generic proxy (cp.async); P by tcgen05.st
-            fence_proxy_async_smem();
-            tc::fence_after_sync();
-            const uint64_t bv = dv[sp];
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              tc::mma_f16_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, bv + (kk * 2048 >> 4),
-                             idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-            if (t == nt - 1) tc::mma_commit(&B->v_empty[sp]);
-            if (j == n_tiles) tc::mma_commit(&B->o_done[t]);
+        if (j >= 1) {
+          const int jp = j - 1;
+          const int sp = jp % kStagesV;
+          ok = wait_or_abort(&B->p_full[t], jp & 1, B, p.error_word) &&
+               wait_or_abort(&B->v_full[sp], (jp / kStagesV) & 1, B, p.error_word);
+          if (!ok) break;
+          if ((L & (kPage - 1)) != 0 && jp == (L - 1) / kBN) {
+            // rows L .. end of the last page hold pool slots past the
+            // sequence: zero them (both 64-dim halves) before P.V reads them
+            // (both issuers write the same zeros)
+            uint8_t* vt = smem + SmemLayout::v + sp * kTileBytes;
+            const int r0 = L - jp * kBN, r1 = ((L + kPage - 1) / kPage) * kPage - jp * kBN;
+            for (int rw = r0; rw < r1; ++rw)
+              for (int c = 0; c < 8; ++c) {
+                *reinterpret_cast<uint4*>(vt + rw * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(vt + kHalf + rw * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+              }
           }
-          if (j < n_tiles) {
-            if (t == 0) {
-              ok = wait_or_abort(&B->k_full[s], (j / kStages) & 1, B, p.error_word);
-              if (!ok) break;
-              fence_proxy_async_smem();
-            }
-            const uint64_t aq = t ? dq[1] : dq[0];
-            const uint64_t bk = dk[s];
+          // zeroed rows (generic proxy) and P (tcgen05.st) before the MMA reads
+          fence_proxy_async_smem();
+          tc::fence_after_sync();
+          const uint64_t bv = dv0 + sp * kTileDesc;
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-              tc::mma_f16(tmem + col_s(t), aq + off, bk + off, idesc_qk, kk > 0);
-            }
-            tc::mma_commit(&B->s_full[t]);
-            if (t == nt - 1) tc::mma_commit(&B->k_empty[s]);
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            tc::mma_f16_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, bv + (kk * 2048 >> 4),
+                           idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(&B->v_empty[sp]);
+          if (j == n_tiles) tc::mma_commit(&B->o_done[t]);
+        }
+        if (j < n_tiles) {
+          const int s = j % kStagesK;
+          ok = wait_or_abort(&B->k_full[s], (j / kStagesK) & 1, B, p.error_word);
+          if (!ok) break;
+          const uint64_t bk = dk0 + s * kTileDesc;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+            tc::mma_f16(tmem + col_s(t), aq + off, bk + off, idesc_qk, kk > 0);
           }
+          tc::mma_commit(&B->s_full[t]);
+          tc::mma_commit(&B->k_empty[s]);
         }
       }
       // drain: all issued MMAs complete before tensor memory is released
-      tc::mma_commit(&B->drain);
-      mbar_wait(&B->drain, 0);
+      tc::mma_commit(&B->drain[t]);
+      mbar_wait(&B->drain[t], 0);
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -351,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(qs + (c >> 3) * kHalf + swz(row, c & 7)) = v;
       }
       fence_proxy_async_smem();
-      asm volatile("bar.sync 1, 288;" ::: "memory");
+      asm volatile("bar.sync 1, 320;" ::: "memory");
     }
     const bool active = t == 0 || has_t1;
     const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -360,6 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl = p.scale_log2;
     bool ok = active;
     for (int j = 0; j < n_tiles && ok; ++j) {
+      // the two warpgroups take turns (softmax 0 of tile j, softmax 1 of
+      // tile j, softmax 0 of tile j + 1, ...), so each runs alone on the
+      // SM's exp and FMA units while the tensor core works for the other
+      if (has_t1 && (t == 1 || j >= 1)) {
+        const bool tw = __all_sync(0xffffffffu, t == 0 ? mbar_wait(&B->p_full[1], (j - 1) & 1)
+                                                     : mbar_wait(&B->p_full[0], j & 1));
+        if (!tw) { abort_cta(B, p.error_word); ok = false; break; }
+      }
       bool w = __all_sync(0xffffffffu, mbar_wait(&B->s_full[t], j & 1));
       if (!w) { abort_cta(B, p.error_word); ok = false; break; }
       tc::fence_after_sync();
@@ -461,6 +466,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------- host
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D view of a cache as [num_blocks * Hkv * 16 rows][128 dims] bf16; box 16
+// rows x 64 dims (128 bytes) with the 128-byte swizzle; rows past the end
+// read as zeros.
+cb_status make_cache_map(CUtensorMap* m, const void* base, int64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return CB_OK;
+}
 }  // namespace prefill
 
 bool prefill_supported(int group) {
@@ -483,7 +523,13 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
                                 (int)smem);
   });
   if (attr != cudaSuccess) return fail(CB_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(attr));
+  const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * kPage;
+  if (rows >= ((int64_t)1 << 31) - kPage) return CB_ERR_UNSUPPORTED;
   Params p{};
+  cb_status st = make_cache_map(&p.tmap_k, a.k_cache, rows);
+  if (st != CB_OK) return st;
+  st = make_cache_map(&p.tmap_v, a.v_cache, rows);
+  if (st != CB_OK) return st;
   p.k_cache = a.k_cache;
   p.v_cache = a.v_cache;
   p.q = static_cast<const __nv_bfloat16*>(a.q);

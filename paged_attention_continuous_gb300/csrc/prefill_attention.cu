@@ -130,11 +130,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// 2^x for a pair of f16 values with one hardware op (ex2.approx.f16x2).
-__device__ __forceinline__ __half2 fast_exp2_h2(__half2 x) {
-  uint32_t xi = *reinterpret_cast<uint32_t*>(&x), yi;
-  asm("ex2.approx.f16x2 %0, %1;" : "=r"(yi) : "r"(xi));
-  return *reinterpret_cast<__half2*>(&yi);
+// 2^x for a pair of bf16 values (low half first) with one hardware op
+// (ex2.approx.ftz.bf16x2); 2^-inf = 0.
+__device__ __forceinline__ uint32_t fast_exp2_bf16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
@@ -380,40 +387,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kBN; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
       }
+      // row max in 8 chains of 3-input max
       float mx[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = sv[u];
+      for (int u = 0; u < 8; ++u) mx[u] = fmax3(sv[u], sv[8 + u], sv[16 + u]);
 #pragma unroll
-      for (int i = 8; i < kBN; i += 8)
+      for (int i = 24; i + 16 <= kBN; i += 16)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], sv[i + u]);
-      const float mt_max =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl;
+        for (int u = 0; u < 8; ++u) mx[u] = fmax3(mx[u], sv[i + u], sv[i + 8 + u]);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], sv[kBN - 8 + u]);
+      const float mt_max = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7])) * sl;
       const float m_new = fmaxf(m_run, mt_max);
       const bool resc = (m_new - m_run) > 8.f;   // also true on the first tile
       const float m_use = resc ? m_new : m_run;  // weights stay <= 2^8 otherwise
       const float alpha = resc ? fast_exp2(m_run - m_use) : 1.f;
       m_run = m_use;
-      // p = 2^(s*scale - m) (one FFMA + one ex2 per score), row sum in 8
-      // chains, P as bf16 pairs written over the S columns (all read above)
-      const float nm = -m_use;
-      float ls[8];
+      // p = 2^(s*scale - m) for a pair of scores at a time: one packed FMA,
+      // the pair rounded to bf16, one packed bf16 ex2 -- which is already P
+      // in the bf16 layout the P.V MMA reads.  The row sum adds exactly those
+      // bf16 values in fp32 (4 packed chains).  P is written over the S
+      // columns (all read above).
+      const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(-m_use, -m_use);
+      float2 ls2[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ls[u] = 0.f;
+      for (int u = 0; u < 4; ++u) ls2[u] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float a = fast_exp2(fmaf(sv[32 * h + i], sl, nm));
-          const float c = fast_exp2(fmaf(sv[32 * h + i + 1], sl, nm));
-          ls[(i >> 1) & 7] += a + c;
-          pk[i / 2] = float2_to_bf16x2(a, c);
+          const float2 x2 = __ffma2_rn(make_float2(sv[32 * h + i], sv[32 * h + i + 1]), sl2, nm2);
+          const uint32_t pb = fast_exp2_bf16x2(float2_to_bf16x2(x2.x, x2.y));
+          pk[i / 2] = pb;
+          ls2[(i >> 1) & 3] = __fadd2_rn(ls2[(i >> 1) & 3], bf16x2_to_float2(pb));
         }
         tc::tmem_st16(trow + colS + 16 * h, pk);
       }
-      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      const float lsum = ((ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y)) +
+                         ((ls2[2].x + ls2[2].y) + (ls2[3].x + ls2[3].y));
       l_run = l_run * alpha + lsum;
       // S_t(j) ready implies P_t.V(j-1) completed (same issuing thread, in
       // order), so O_t is stable here and may be rescaled.

@@ -44,10 +44,10 @@ import workloads  # noqa: E402
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the
-# decode kernel on the mixed 2048-token step (1.72 GB read + 7.64 MB
-# written, as ncu prints them); reported only for that workload and set back
-# to None whenever the kernel changes.
-DECODE_TRAFFIC_BYTES = {"mixed_2048": 1.72e9 + 7.64e6}
+# decode kernel per workload (as ncu prints them: mixed 2048-token step 1.72
+# GB read + 10.32 MB written; 64-request decode step 566.31 MB + 8.71 MB);
+# cleared whenever the kernel changes.
+DECODE_TRAFFIC_BYTES = {"mixed_2048": 1.72e9 + 10.32e6, "decode_64": 566.31e6 + 8.71e6}
 
 
 def peaks():

@@ -348,6 +348,97 @@ def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
             "sampled_steps": per_step, "reps_per_step": reps}
 
 
+def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000):
+    """Request trace: 2,000 requests with Poisson(20) arrivals per step and
+    lognormal prompt / output lengths (medians 512 / 128), 4 layers each with
+    its own 65,536-block pool, budget 8,192 tokens and 256 requests per step,
+    run until every request has finished.  Per step: the host scheduler call
+    (timed on the host), one metadata upload, and per layer the step's fresh
+    q/k/v (drawn per (step, layer), untimed) then append + attention (timed
+    with CUDA events).  Reports whole-trace tokens/s, the additive roofline
+    fraction (decode bytes / HBM peak + prefill FLOPs / tensor peak, over the
+    measured kernel time) and the KV-block fragmentation (slots allocated but
+    not yet holding a token, over all allocated slots, mean over steps)."""
+    from paged_attention_continuous_gb300.step import StepRunner
+    sc = workloads.trace_2000()
+    s = cb.Scheduler(block_size=sc.block_size, num_blocks=sc.num_blocks,
+                     max_batch_tokens=sc.max_batch_tokens,
+                     max_requests_per_batch=sc.max_requests_per_batch,
+                     max_blocks_per_seq=sc.max_blocks_per_seq,
+                     max_prefill_chunk=sc.max_prefill_chunk, safety_margin=sc.safety_margin,
+                     free_list=sc.free_list)
+    runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
+                        num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim, dtype=sc.dtype,
+                        max_reqs=sc.max_requests_per_batch, max_tokens=sc.max_batch_tokens,
+                        max_blocks_per_seq=sc.max_blocks_per_seq, num_layers=sc.num_layers,
+                        device=dev)
+    events = []
+    t_host = 0.0
+    tokens = 0
+    d_bytes = 0
+    p_flops = 0
+    frag = []
+    finished = 0
+    nxt = 0
+    step = 0
+    stalled_steps = 0
+    while finished < len(sc.waiting) and step < max_steps:
+        while nxt < len(sc.waiting) and sc.waiting[nxt].arrival_step <= step:
+            w = sc.waiting[nxt]
+            s.add_request(w.req_id, w.prompt_len, w.output_len)
+            nxt += 1
+        h0 = time.perf_counter()
+        st = s.schedule_step()
+        t_host += time.perf_counter() - h0
+        if st["status"] != 0 or st["num_reqs"] == 0:
+            stalled_steps += 1
+            step += 1
+            continue
+        T = st["num_tokens"]
+        ds = runner.upload(st)
+        for layer in range(sc.num_layers):
+            sd = [workloads.step_seed(sc.seed, step, layer, c) for c in range(3)]
+            q = workloads.token_tensors(T, sc.num_q_heads, sc.head_dim, seed=sd[0], dtype=sc.dtype,
+                                        scale=sc.value_scale, device=dev)
+            k = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=sd[1], dtype=sc.dtype,
+                                        scale=sc.value_scale, device=dev)
+            v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=sd[2], dtype=sc.dtype,
+                                        scale=sc.value_scale, device=dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            runner.run(ds, q, k, v, layer=layer)
+            e1.record()
+            events.append((e0, e1))
+        h0 = time.perf_counter()
+        finished += len(s.step_done())
+        t_host += time.perf_counter() - h0
+        tokens += T
+        d_bytes += sc.num_layers * decode_bytes(st, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, 2)
+        p_flops += sc.num_layers * prefill_flops(st, sc.num_q_heads, sc.head_dim)
+        sl = np.asarray(st["seq_lens"], dtype=np.int64)
+        alloc = ((sl + sc.block_size - 1) // sc.block_size) * sc.block_size
+        frag.append(float((alloc - sl).sum() / max(alloc.sum(), 1)))
+        step += 1
+    torch.cuda.synchronize()
+    t_dev = sum(a.elapsed_time(b) for a, b in events) / 1e3
+    assert runner.workspace.read_errors() == 0
+    del runner
+    torch.cuda.empty_cache()
+    t_roof = d_bytes / (hbm * 1e9) + p_flops / (bf16 * 1e12)
+    return {"workload": "trace_2000 (2,000 requests, Poisson(20) arrivals, lognormal lengths, "
+                        "4 layers x 65,536 blocks, 32Q/8KV, D=128, budget 8192 / 256 reqs)",
+            "steps": step, "steps_without_batch": stalled_steps, "finished": finished,
+            "tokens": int(tokens),
+            "tokens_per_s_device": round(tokens / t_dev, 1) if t_dev else 0.0,
+            "tokens_per_s_with_host_scheduler": round(tokens / (t_dev + t_host), 1),
+            "ms_device_total": round(t_dev * 1e3, 2), "ms_host_scheduler_total": round(t_host * 1e3, 2),
+            "decode_bytes": int(d_bytes), "prefill_flops": int(p_flops),
+            "roofline_frac_additive": round(t_roof / t_dev, 4) if t_dev else 0.0,
+            "fragmentation_mean": round(float(np.mean(frag)) if frag else 0.0, 4),
+            "timed": "per layer: cb_kv_append + cb_paged_attention (CUDA events); "
+                     "scheduler calls on the host; q/k/v generation untimed"}
+
+
 # ----------------------------------------------------------- CPU oracle
 def oracle_sample(sc, step, pools_cpu, rows, prefill_token_cap=None):
     """Run the oracle on ``rows`` of ``step``: gather each row's cache blocks
@@ -566,6 +657,7 @@ def run_ours(args, rank, world):
     if not args.no_extra and world == 1:
         line["decode_only"] = measure_decode_only(cb, torch, dev, max(K, 20), hbm)
         line["long_prompt"] = measure_long_prompt(cb, torch, dev, 3, hbm, bf16, bf16s)
+        line["trace"] = measure_trace(cb, torch, dev, hbm, bf16)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sc, step, runner, q, k, v, torch, dev,
                                             budget_s=args.cpu_seconds)

@@ -249,7 +249,8 @@ typedef struct cb_attention_args {
 #define CB_DEVERR_BLOCK_RANGE 0x1u  /* block id outside [0, num_blocks) */
 #define CB_DEVERR_SLOT_RANGE 0x2u   /* slot outside the cache */
 #define CB_DEVERR_DECODE_QLEN 0x4u  /* a decode row with query length != 1 */
-#define CB_DEVERR_SEQ_RANGE 0x8u    /* seq_len < q_len or beyond the table */
+#define CB_DEVERR_SEQ_RANGE 0x8u    /* seq_len < q_len, beyond the table, or a
+                                       row's queries outside [0, num_tokens) */
 #define CB_DEVERR_TIMEOUT 0x10u     /* a bounded wait ran out */
 #define CB_DEVERR_PLAN 0x20u        /* decode splits did not fit the partial slots */
 

@@ -106,6 +106,7 @@ struct Params {
   const int32_t* seq_lens;
   const int32_t* block_tables;
   int32_t row_begin;          // first prefill row
+  int32_t num_tokens;         // rows of q / out
   int32_t num_blocks, max_blocks_per_seq, num_q_heads, num_kv_heads, group;
   float scale_log2;
   uint32_t* error_word;
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_len = p.cu_seqlens_q[r + 1] - q0;
   const int L = p.seq_lens[r];
   const int W = p.max_blocks_per_seq;
-  if (q_len < 1 || L < q_len || (L + kPage - 1) / kPage > W) {
+  if (q_len < 1 || q0 < 0 || q0 + q_len > p.num_tokens || L < q_len || (L + kPage - 1) / kPage > W) {
     if (threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && g == 0)
       set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
     return;
@@ -551,6 +552,7 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   p.seq_lens = a.seq_lens;
   p.block_tables = a.block_tables;
   p.row_begin = a.num_decodes;
+  p.num_tokens = a.num_tokens;
   p.num_blocks = a.num_blocks;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.num_q_heads = a.num_q_heads;

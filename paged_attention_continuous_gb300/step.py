@@ -54,10 +54,19 @@ class StepRunner:
         self.v_cache = [alloc(shape, dtype=self.dt, device=device) for _ in range(num_layers)]
         self.workspace = Workspace(max_reqs, num_q_heads, num_kv_heads, head_dim, device=device)
         cap = (max_reqs + 1) + max_reqs + max_reqs * max_blocks_per_seq + max_tokens
-        self._host = torch.empty(cap, dtype=torch.int32, pin_memory=True)
+        # two pinned staging buffers, used in turn: a buffer is refilled only
+        # after the copy that last read it has executed (its event), since
+        # the host may run steps ahead of the device
+        self._host = [torch.empty(cap, dtype=torch.int32, pin_memory=True) for _ in range(2)]
+        self._copied = [None, None]
+        self._turn = 0
         self._dev = torch.empty(cap, dtype=torch.int32, device=device)
 
     def upload(self, step: dict, stream=None) -> DeviceStep:
+        """Copy a step's metadata to the device (one pinned copy on the
+        current stream).  The returned arrays stay valid until the next
+        upload on this runner; kernels that use them must be queued on the
+        same stream before that next upload."""
         R, T = int(step["num_reqs"]), int(step["num_tokens"])
         if R > self.max_reqs or T > self.max_tokens:
             raise ValueError("step larger than the runner was sized for")
@@ -66,13 +75,20 @@ class StepRunner:
         if bt.shape[1] != W:
             raise ValueError("block_tables width differs from max_blocks_per_seq")
         n = (R + 1) + R + R * W + T
-        h = self._host.numpy()
+        b = self._turn
+        self._turn ^= 1
+        if self._copied[b] is not None:
+            self._copied[b].synchronize()
+        h = self._host[b].numpy()
         o = 0
         h[o:o + R + 1] = step["cu_seqlens_q"]; o1 = o + R + 1
         h[o1:o1 + R] = step["seq_lens"]; o2 = o1 + R
         h[o2:o2 + R * W] = bt.reshape(-1); o3 = o2 + R * W
         h[o3:o3 + T] = step["slot_mapping"]
-        self._dev[:n].copy_(self._host[:n], non_blocking=True)
+        self._dev[:n].copy_(self._host[b][:n], non_blocking=True)
+        ev = self.torch.cuda.Event()
+        ev.record()
+        self._copied[b] = ev
         d = self._dev
         return DeviceStep(R, T, int(step["num_decodes"]), int(step["max_q_len"]) if "max_q_len" in step
                           else int(np.diff(step["cu_seqlens_q"]).max(initial=1)),

@@ -32,7 +32,11 @@ def tolerance_ok(gpu: np.ndarray, ref: np.ndarray, dtype: str):
 
 
 class ParityRun:
-    def __init__(self, sc, sample=None, device="cuda", fill_seed=1234, max_tokens=None):
+    """``arrivals``: add each waiting request before the step numbered by its
+    arrival_step (a trace), instead of all of them up front."""
+
+    def __init__(self, sc, sample=None, device="cuda", fill_seed=1234, max_tokens=None,
+                 arrivals=False):
         import paged_attention_continuous_gb300 as cb
         from paged_attention_continuous_gb300.step import StepRunner
         self.sc = sc
@@ -45,8 +49,15 @@ class ParityRun:
                               max_blocks_per_seq=cfg["max_blocks_per_seq"],
                               max_prefill_chunk=cfg["max_prefill_chunk"],
                               safety_margin=cfg["safety_margin"], free_list=cfg["free_list"])
-        load_scenario(self.o, sc)
-        load_scenario(self.c, sc)
+        self.arrivals = arrivals
+        self.next_arrival = 0
+        if arrivals:
+            for sched in (self.o, self.c):
+                for r in sc.running:
+                    sched.add_running_request(r.req_id, r.prompt_len, r.output_len, r.num_cached)
+        else:
+            load_scenario(self.o, sc)
+            load_scenario(self.c, sc)
         self.runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
                                  num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim,
                                  dtype=sc.dtype, max_reqs=sc.max_requests_per_batch,
@@ -94,11 +105,19 @@ class ParityRun:
         """One step on both sides.  Returns (status, gpu_out[layer] as float64
         numpy for followed rows, oracle_out[layer], followed token indices)."""
         sc = self.sc
+        if self.arrivals:
+            while (self.next_arrival < len(sc.waiting) and
+                   sc.waiting[self.next_arrival].arrival_step <= self.step_idx):
+                w = sc.waiting[self.next_arrival]
+                self.o.add_request(w.req_id, w.prompt_len, w.output_len)
+                self.c.add_request(w.req_id, w.prompt_len, w.output_len)
+                self.next_arrival += 1
         so = self.o.schedule_step()
         sg = self.c.schedule_step()
         self.last = so
         assert normalize(so) == normalize(sg), "schedulers disagree"
         if so["status"] != 0:
+            self.step_idx += 1
             return so["status"], None, None, None
         T = so["num_tokens"]
         rows = [i for i, rid in enumerate(so["req_ids"]) if self._followed(rid)]

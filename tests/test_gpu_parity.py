@@ -258,6 +258,24 @@ def test_full_long_prompt_late_step_sampled():
     _check(g[0], r[0], "bf16", "long prompt step 6")
 
 
+def test_trace_first_steps_sampled_all_layers():
+    """The request trace (Poisson arrivals, lognormal lengths, 4 layers with
+    their own pools): its first 10 steps with arrivals added per step; the
+    oracle follows four short requests (two arriving at step 0, one at 1,
+    one at 2) through prefill and decode on every layer."""
+    sc = workloads.trace_2000()
+    run = ParityRun(sc, sample=[1, 5, 25, 39], arrivals=True)
+    seen = 0
+    for step in range(10):
+        st, g, r, toks = run.step()
+        assert st == 0
+        for layer in range(sc.num_layers):
+            if len(toks):
+                _check(g[layer], r[layer], "bf16", f"trace step {step} layer {layer}")
+        seen += len(toks)
+    assert seen > 0
+
+
 def test_empty_batch_is_a_noop():
     cb = _cb()
     ws = cb.Workspace(4, 8, 8, 128)

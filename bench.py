@@ -348,7 +348,7 @@ def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
             "sampled_steps": per_step, "reps_per_step": reps}
 
 
-def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000):
+def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000, graphs=False):
     """Request trace: 2,000 requests with Poisson(20) arrivals per step and
     lognormal prompt / output lengths (medians 512 / 128), 4 layers each with
     its own 65,536-block pool, budget 8,192 tokens and 256 requests per step,
@@ -358,8 +358,11 @@ def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000):
     with CUDA events).  Reports whole-trace tokens/s, the additive roofline
     fraction (decode bytes / HBM peak + prefill FLOPs / tensor peak, over the
     measured kernel time) and the KV-block fragmentation (slots allocated but
-    not yet holding a token, over all allocated slots, mean over steps)."""
-    from paged_attention_continuous_gb300.step import StepRunner
+    not yet holding a token, over all allocated slots, mean over steps).
+    With ``graphs`` every step (all layers) is one CUDA-graph replay of its
+    padded bucket (GraphStepRunner); q/k/v are copied into its static
+    buffers outside the timed replay."""
+    from paged_attention_continuous_gb300.step import GraphStepRunner, StepRunner
     sc = workloads.trace_2000()
     s = cb.Scheduler(block_size=sc.block_size, num_blocks=sc.num_blocks,
                      max_batch_tokens=sc.max_batch_tokens,
@@ -367,11 +370,12 @@ def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000):
                      max_blocks_per_seq=sc.max_blocks_per_seq,
                      max_prefill_chunk=sc.max_prefill_chunk, safety_margin=sc.safety_margin,
                      free_list=sc.free_list)
-    runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
-                        num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim, dtype=sc.dtype,
-                        max_reqs=sc.max_requests_per_batch, max_tokens=sc.max_batch_tokens,
-                        max_blocks_per_seq=sc.max_blocks_per_seq, num_layers=sc.num_layers,
-                        device=dev)
+    Runner = GraphStepRunner if graphs else StepRunner
+    runner = Runner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
+                    num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim, dtype=sc.dtype,
+                    max_reqs=sc.max_requests_per_batch, max_tokens=sc.max_batch_tokens,
+                    max_blocks_per_seq=sc.max_blocks_per_seq, num_layers=sc.num_layers,
+                    device=dev)
     events = []
     t_host = 0.0
     tokens = 0
@@ -395,7 +399,10 @@ def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000):
             step += 1
             continue
         T = st["num_tokens"]
-        ds = runner.upload(st)
+        if graphs:
+            key, _ = runner.prepare(st)
+        else:
+            ds = runner.upload(st)
         for layer in range(sc.num_layers):
             sd = [workloads.step_seed(sc.seed, step, layer, c) for c in range(3)]
             q = workloads.token_tensors(T, sc.num_q_heads, sc.head_dim, seed=sd[0], dtype=sc.dtype,
@@ -404,9 +411,20 @@ def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000):
                                         scale=sc.value_scale, device=dev)
             v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=sd[2], dtype=sc.dtype,
                                         scale=sc.value_scale, device=dev)
+            if graphs:
+                runner.q_buf[layer][:T].copy_(q)
+                runner.k_buf[layer][:T].copy_(k)
+                runner.v_buf[layer][:T].copy_(v)
+                continue
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             runner.run(ds, q, k, v, layer=layer)
+            e1.record()
+            events.append((e0, e1))
+        if graphs:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            runner.run(key)
             e1.record()
             events.append((e0, e1))
         h0 = time.perf_counter()
@@ -422,10 +440,12 @@ def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000):
     torch.cuda.synchronize()
     t_dev = sum(a.elapsed_time(b) for a, b in events) / 1e3
     assert runner.workspace.read_errors() == 0
+    n_graphs = len(runner.graphs) if graphs else 0
     del runner
     torch.cuda.empty_cache()
     t_roof = d_bytes / (hbm * 1e9) + p_flops / (bf16 * 1e12)
-    return {"workload": "trace_2000 (2,000 requests, Poisson(20) arrivals, lognormal lengths, "
+    return {"graphs": n_graphs if graphs else None,
+            "workload": "trace_2000 (2,000 requests, Poisson(20) arrivals, lognormal lengths, "
                         "4 layers x 65,536 blocks, 32Q/8KV, D=128, budget 8192 / 256 reqs)",
             "steps": step, "steps_without_batch": stalled_steps, "finished": finished,
             "tokens": int(tokens),
@@ -658,6 +678,7 @@ def run_ours(args, rank, world):
         line["decode_only"] = measure_decode_only(cb, torch, dev, max(K, 20), hbm)
         line["long_prompt"] = measure_long_prompt(cb, torch, dev, 3, hbm, bf16, bf16s)
         line["trace"] = measure_trace(cb, torch, dev, hbm, bf16)
+        line["trace_graphs"] = measure_trace(cb, torch, dev, hbm, bf16, graphs=True)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sc, step, runner, q, k, v, torch, dev,
                                             budget_s=args.cpu_seconds)

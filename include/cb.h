@@ -216,6 +216,10 @@ cb_status cb_kv_append(const void* k_new, const void* v_new,
  * Rows [0, num_decodes) must have query length 1 and run the split-KV decode
  * kernel (which also merges the splits of requests whose cache it split);
  * the remaining rows run the prefill-chunk kernel.  Both go to `stream`.
+ * A row with query length 0 and seq_len 0 is padding and is skipped (no
+ * error bit), so a step may be padded to a fixed shape (row counts, token
+ * count, max_q_len) and captured once in a CUDA graph; padded tokens carry
+ * slot -1 for cb_kv_append.
  * ---------------------------------------------------------------------- */
 typedef struct cb_attention_args {
   const void* q;                /* device [num_tokens][Hq][D] */

@@ -220,13 +220,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
     const int q0 = p.cu_seqlens_q[r];
     const int q1 = p.cu_seqlens_q[r + 1];
     int pages = (L + kPageTokens - 1) / kPageTokens;
-    if (L < 1 || pages > W) {
-      L = 0;
-      if (blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
-    }
-    if (q1 - q0 != 1 || q0 < 0 || q0 >= p.num_tokens) {
-      L = 0;
-      if (blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_DECODE_QLEN);
+    if (L == 0 && q1 == q0) {
+      // a padding row (no query, no context): nothing to do
+    } else {
+      if (L < 1 || pages > W) {
+        L = 0;
+        if (blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
+      }
+      if (q1 - q0 != 1 || q0 < 0 || q0 >= p.num_tokens) {
+        L = 0;
+        if (blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_DECODE_QLEN);
+      }
     }
     pages = (L + kPageTokens - 1) / kPageTokens;
     row_len[i] = L;

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_len = p.cu_seqlens_q[r + 1] - q0;
   const int L = p.seq_lens[r];
   const int W = p.max_blocks_per_seq;
+  if (q_len == 0 && L == 0) return;  // a padding row
   if (q_len < 1 || q0 < 0 || q0 + q_len > p.num_tokens || L < q_len || (L + kPage - 1) / kPage > W) {
     if (threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && g == 0)
       set_error(p.error_word, CB_DEVERR_SEQ_RANGE);

@@ -106,3 +106,146 @@ class StepRunner:
                                num_decodes=ds.num_decodes, max_q_len=ds.max_q_len,
                                max_seq_len=ds.max_seq_len, scale=self.scale,
                                workspace=self.workspace, out=out)
+
+
+def bucket(n: int, lo: int = 1) -> int:
+    """Smallest power of two >= n (>= lo); 0 for n <= 0."""
+    if n <= 0:
+        return 0
+    b = lo
+    while b < n:
+        b *= 2
+    return b
+
+
+class GraphStepRunner:
+    """A whole step -- every layer's cb_kv_append + cb_paged_attention --
+    replayed from a CUDA graph.
+
+    "Continuous batching architecture" (HF Transformers docs) pads a step's
+    shapes to a few intervals so that captured graphs can be reused; here
+    the step is padded up to power-of-two buckets of (tokens, decode rows,
+    prefill rows, longest prefill chunk).  Padding rows have query length 0
+    and seq_len 0 (the kernels skip them), padding tokens slot -1 (the append
+    skips them), so one graph per bucket serves every step that fits it.  A
+    graph is captured the first time its bucket is met, after one uncaptured
+    run of the same launches.
+
+    Per step: ``prepare(step)`` pads and uploads the metadata (one pinned
+    copy into a static device buffer, two pinned buffers used in turn) and
+    returns the bucket; the caller writes the step's q/k/v rows into
+    ``q_buf[layer][:T]``, ``k_buf[layer][:T]``, ``v_buf[layer][:T]``; ``run(key)``
+    replays the graph; the outputs are ``out_buf[layer][:T]``.
+    """
+
+    def __init__(self, *, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                 dtype: str, max_reqs: int, max_tokens: int, max_blocks_per_seq: int,
+                 num_layers: int = 1, block_size: int = 16, device: str = "cuda",
+                 scale: Optional[float] = None, zero_cache: bool = True):
+        import torch
+        self.torch = torch
+        self.dt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
+        self.Hq, self.Hkv, self.D = num_q_heads, num_kv_heads, head_dim
+        self.block_size = block_size
+        self.W = max_blocks_per_seq
+        self.L = num_layers
+        self.scale = 1.0 / math.sqrt(head_dim) if scale is None else scale
+        self.R_cap = 2 * bucket(max_reqs)     # padded decode rows + padded prefill rows
+        self.T_cap = bucket(max_tokens, 16)
+        alloc = torch.zeros if zero_cache else torch.empty
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        self.k_cache = [alloc(shape, dtype=self.dt, device=device) for _ in range(num_layers)]
+        self.v_cache = [alloc(shape, dtype=self.dt, device=device) for _ in range(num_layers)]
+        self.workspace = Workspace(self.R_cap, num_q_heads, num_kv_heads, head_dim, device=device)
+        mk = lambda h: [torch.zeros(self.T_cap, h, head_dim, dtype=self.dt, device=device)
+                        for _ in range(num_layers)]
+        self.q_buf, self.k_buf, self.v_buf = mk(num_q_heads), mk(num_kv_heads), mk(num_kv_heads)
+        self.out_buf = mk(num_q_heads)
+        cap = (self.R_cap + 1) + self.R_cap + self.R_cap * self.W + self.T_cap
+        self._host = [torch.empty(cap, dtype=torch.int32, pin_memory=True) for _ in range(2)]
+        self._copied = [None, None]
+        self._turn = 0
+        self._dev = torch.empty(cap, dtype=torch.int32, device=device)
+        self.graphs = {}
+        self.pool = None
+
+    def prepare(self, step: dict):
+        """Pad the step to its bucket and upload it; returns (key, T)."""
+        R, T, nd = int(step["num_reqs"]), int(step["num_tokens"]), int(step["num_decodes"])
+        npf = R - nd
+        cu = np.asarray(step["cu_seqlens_q"], dtype=np.int64)
+        max_q = int(np.diff(cu[nd:]).max(initial=0)) if npf else 0
+        key = (bucket(T, 16), bucket(nd), bucket(npf), bucket(max_q))
+        Tb, ndb, npb, _ = key
+        Rb = ndb + npb
+        if Tb > self.T_cap or Rb > self.R_cap:
+            raise ValueError("step larger than the runner was sized for")
+        W = self.W
+        bt = np.asarray(step["block_tables"], dtype=np.int32).reshape(R, -1)
+        if bt.shape[1] != W:
+            raise ValueError("block_tables width differs from max_blocks_per_seq")
+        b = self._turn
+        self._turn ^= 1
+        if self._copied[b] is not None:
+            self._copied[b].synchronize()
+        h = self._host[b].numpy()
+        o_cu, o_sl, o_bt, o_sm = 0, Rb + 1, 2 * Rb + 1, 2 * Rb + 1 + Rb * W
+        n = o_sm + Tb
+        # rows: real decodes, decode padding, real prefills, prefill padding
+        rows = list(range(nd)) + [-1] * (ndb - nd) + list(range(nd, R)) + [-1] * (npb - npf)
+        cu_p = np.empty(Rb + 1, dtype=np.int32)
+        sl_p = np.zeros(Rb, dtype=np.int32)
+        bt_p = np.full((Rb, W), -1, dtype=np.int32)
+        tok = 0
+        for i, r in enumerate(rows):
+            cu_p[i] = tok
+            if r >= 0:
+                tok = int(cu[r + 1])
+                sl_p[i] = step["seq_lens"][r]
+                bt_p[i] = bt[r]
+        cu_p[Rb] = tok
+        h[o_cu:o_cu + Rb + 1] = cu_p
+        h[o_sl:o_sl + Rb] = sl_p
+        h[o_bt:o_bt + Rb * W] = bt_p.reshape(-1)
+        h[o_sm:o_sm + T] = step["slot_mapping"]
+        h[o_sm + T:o_sm + Tb] = -1
+        self._dev[:n].copy_(self._host[b][:n], non_blocking=True)
+        ev = self.torch.cuda.Event()
+        ev.record()
+        self._copied[b] = ev
+        return key, T
+
+    def _launch(self, key):
+        Tb, ndb, npb, mqb = key
+        Rb = ndb + npb
+        W = self.W
+        d = self._dev
+        cu, sl = d[0:Rb + 1], d[Rb + 1:2 * Rb + 1]
+        bt = d[2 * Rb + 1:2 * Rb + 1 + Rb * W].view(Rb, W)
+        sm = d[2 * Rb + 1 + Rb * W:2 * Rb + 1 + Rb * W + Tb]
+        for layer in range(self.L):
+            kc, vc = self.k_cache[layer], self.v_cache[layer]
+            kv_append(self.k_buf[layer][:Tb], self.v_buf[layer][:Tb], sm, kc, vc)
+            paged_attention(self.q_buf[layer][:Tb], kc, vc, cu, sl, bt, num_decodes=ndb,
+                            max_q_len=max(mqb, 1), max_seq_len=W * self.block_size,
+                            scale=self.scale, workspace=self.workspace,
+                            out=self.out_buf[layer][:Tb])
+
+    def run(self, key):
+        """Run the step last prepared (key from prepare)."""
+        torch = self.torch
+        g = self.graphs.get(key)
+        if g is not None:
+            g.replay()
+            return
+        # first step of this bucket: run it uncaptured (this also does the
+        # library's one-time set-up), then record the same launches; the
+        # capture does not execute them, so the step runs once
+        self._launch(key)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, pool=self.pool):
+            self._launch(key)
+        if self.pool is None:
+            self.pool = g.pool()
+        self.graphs[key] = g

@@ -109,7 +109,26 @@ typedef struct cb_config {
                                        distinct ids in [0, num_blocks): the
                                        allocation order; NULL = 0,1,2,...
                                        Copied; not retained. */
+  int32_t policy;                 /* CB_POLICY_FIFO (0, default): decodes,
+                                     running prefills, new prompts;
+                                     CB_POLICY_PREFILL_FIRST (1): running
+                                     prefills, new prompts, then decodes with
+                                     what is left ("Continuous batching
+                                     architecture", PrefillFirst).  Rows are
+                                     always emitted decodes first. */
+  int32_t max_prefill_reqs;       /* prefill rows (running + new) per step;
+                                     0 = no cap */
+  int32_t long_prefill_tokens;    /* prompts longer than this are "long";
+                                     0 = no long-prefill cap */
+  int32_t max_long_prefills;      /* long requests allowed in their prefill
+                                     phase at once (vLLM post, request-
+                                     parallel prefill); a long waiting
+                                     request held by it is skipped, not
+                                     blocking shorter ones behind it */
 } cb_config;
+
+#define CB_POLICY_FIFO 0
+#define CB_POLICY_PREFILL_FIRST 1
 
 typedef struct cb_sched cb_sched;
 

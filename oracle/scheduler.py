@@ -26,6 +26,11 @@ Follows:
 * *Chunked Prefill* (Ultralytics glossary), "How chunked prefill works": one
   token per running decode first, then chunks of waiting prompts fill the
   remaining budget.
+* *Continuous batching architecture*, "PrefillFirst": chunked prefills are
+  completed before decoding resumes (policy PREFILL_FIRST).
+* vLLM performance-series post (page 5), "Request-parallel prefill": several
+  requests may prefill in one batch, but only a limited number of LONG
+  prompts at a time, so short prompts are not held behind a long one.
 
 Readings where the pages leave a step open:
 
@@ -52,6 +57,17 @@ Readings where the pages leave a step open:
    steps.  A decode step's query token sits at position num_cached and its
    K/V is appended in the same step.
 8. slot = block_table[pos // block_size] * block_size + pos % block_size.
+9. PREFILL_FIRST takes the same three groups in the order running prefills,
+   new prompts, decodes (the decodes get what budget and request cap are
+   left; blocks are taken in that order); the emitted rows stay decodes
+   first (the attention call's layout), then running prefills, then new
+   prompts.
+10. ``max_prefill_reqs`` (0 = none) caps the prefill rows (running + new)
+   of a step.  A prompt is long when prompt_len > ``long_prefill_tokens``
+   (0 = no long cap); a long waiting request is admitted only while fewer
+   than ``max_long_prefills`` long requests are in their prefill phase, and
+   one held by that cap is skipped (keeps its place) instead of blocking
+   the requests behind it.
 
 Parity: pinned by hand-derived traces (tests/golden/scheduler_*.json) and by
 invariants (budget, cap, FIFO order, block conservation, all-or-nothing
@@ -70,6 +86,7 @@ WAITING, PREFILLING, DECODING, FINISHED = "waiting", "prefilling", "decoding", "
 
 STATUS_OK = 0
 STATUS_NO_BLOCKS = 2
+POLICY_FIFO, POLICY_PREFILL_FIRST = 0, 1
 
 
 class Request:
@@ -88,13 +105,19 @@ class FifoScheduler:
                  max_batch_tokens: int, max_requests_per_batch: int,
                  max_blocks_per_seq: int, max_prefill_chunk: int = 0,
                  safety_margin: float = 0.15,
-                 free_list: Optional[Sequence[int]] = None):
+                 free_list: Optional[Sequence[int]] = None,
+                 policy: int = POLICY_FIFO, max_prefill_reqs: int = 0,
+                 long_prefill_tokens: int = 0, max_long_prefills: int = 1):
         self.block_size = int(block_size)
         self.num_blocks = int(num_blocks)
         self.max_batch_tokens = int(max_batch_tokens)
         self.max_requests_per_batch = int(max_requests_per_batch)
         self.max_blocks_per_seq = int(max_blocks_per_seq)
         self.max_prefill_chunk = int(max_prefill_chunk)
+        self.policy = int(policy)
+        self.max_prefill_reqs = int(max_prefill_reqs)
+        self.long_prefill_tokens = int(long_prefill_tokens)
+        self.max_long_prefills = int(max_long_prefills)
         margin32 = float(np.float32(safety_margin))
         self.reserved_blocks = int(math.ceil(margin32 * float(self.num_blocks)))
         if free_list is None:
@@ -154,69 +177,97 @@ class FifoScheduler:
         return out
 
     # ---------------------------------------------------------------- step
+    def _is_long(self, r) -> bool:
+        return self.long_prefill_tokens > 0 and r.prompt_len > self.long_prefill_tokens
+
     def schedule_step(self) -> dict:
         if self._pending is not None:
             raise RuntimeError("schedule_step called twice without step_done")
         budget = self.max_batch_tokens
         cap = self.max_requests_per_batch
-        batch = []            # (request, num_tokens)
-        stalled = []          # (req_id, blocks demanded)
+        mpr = self.max_prefill_reqs
+        dec, pre, new = [], [], []   # (request, num_tokens) per group
+        stalled = []                 # (req_id, blocks demanded)
+        rows = lambda: len(dec) + len(pre) + len(new)
+        prefill_cap_hit = lambda: mpr > 0 and len(pre) + len(new) >= mpr
 
-        # 1) active decodes, one token each, in admission order
-        for r in self.running:
-            if r.state != DECODING:
-                continue
-            if budget == 0 or len(batch) == cap:
-                break
-            need = self._blocks_for(r.num_cached + 1) - len(r.blocks)
-            if need > len(self.free):
-                stalled.append((r.req_id, need))
-                continue
-            for _ in range(need):
-                r.blocks.append(self.free.popleft())
-            batch.append((r, 1))
-            budget -= 1
-        num_decodes = len(batch)
+        def decodes():
+            # active decodes, one token each, in admission order
+            nonlocal budget
+            for r in self.running:
+                if r.state != DECODING:
+                    continue
+                if budget == 0 or rows() == cap:
+                    break
+                need = self._blocks_for(r.num_cached + 1) - len(r.blocks)
+                if need > len(self.free):
+                    stalled.append((r.req_id, need))
+                    continue
+                for _ in range(need):
+                    r.blocks.append(self.free.popleft())
+                dec.append((r, 1))
+                budget -= 1
 
-        # 2) active prefills, next chunk each, in admission order
-        for r in self.running:
-            if r.state != PREFILLING:
-                continue
-            if budget == 0 or len(batch) == cap:
-                break
-            n = min(r.prompt_len - r.num_cached, budget)
-            if self.max_prefill_chunk > 0:
-                n = min(n, self.max_prefill_chunk)
-            need = self._blocks_for(r.num_cached + n) - len(r.blocks)
-            if need > len(self.free):
-                stalled.append((r.req_id, need))
-                continue
-            for _ in range(need):
-                r.blocks.append(self.free.popleft())
-            batch.append((r, n))
-            budget -= n
+        def running_prefills():
+            # active prefills, next chunk each, in admission order
+            nonlocal budget
+            for r in self.running:
+                if r.state != PREFILLING:
+                    continue
+                if budget == 0 or rows() == cap or prefill_cap_hit():
+                    break
+                n = min(r.prompt_len - r.num_cached, budget)
+                if self.max_prefill_chunk > 0:
+                    n = min(n, self.max_prefill_chunk)
+                need = self._blocks_for(r.num_cached + n) - len(r.blocks)
+                if need > len(self.free):
+                    stalled.append((r.req_id, need))
+                    continue
+                for _ in range(need):
+                    r.blocks.append(self.free.popleft())
+                pre.append((r, n))
+                budget -= n
 
-        # 3) waiting requests in arrival order, strict head-of-line
-        while self.waiting and budget > 0 and len(batch) < cap:
-            r = self.waiting[0]
-            n = min(r.prompt_len, budget)
-            if self.max_prefill_chunk > 0:
-                n = min(n, self.max_prefill_chunk)
-            need = self._blocks_for(n)
-            if len(self.free) - need < self.reserved_blocks:
-                break
-            self.waiting.popleft()
-            for _ in range(need):
-                r.blocks.append(self.free.popleft())
-            r.state = PREFILLING
-            self.running.append(r)
-            batch.append((r, n))
-            budget -= n
+        def admissions():
+            # waiting requests in arrival order, head-of-line except for long
+            # prompts held back by the long-prefill cap
+            nonlocal budget
+            i = 0
+            while i < len(self.waiting) and budget > 0 and rows() < cap and not prefill_cap_hit():
+                r = self.waiting[i]
+                if self._is_long(r):
+                    active = sum(1 for x in self.running if x.state == PREFILLING and self._is_long(x))
+                    if active >= self.max_long_prefills:
+                        i += 1
+                        continue
+                n = min(r.prompt_len, budget)
+                if self.max_prefill_chunk > 0:
+                    n = min(n, self.max_prefill_chunk)
+                need = self._blocks_for(n)
+                if len(self.free) - need < self.reserved_blocks:
+                    break
+                del self.waiting[i]
+                for _ in range(need):
+                    r.blocks.append(self.free.popleft())
+                r.state = PREFILLING
+                self.running.append(r)
+                new.append((r, n))
+                budget -= n
+
+        if self.policy == POLICY_PREFILL_FIRST:
+            running_prefills()
+            admissions()
+            decodes()
+        else:
+            decodes()
+            running_prefills()
+            admissions()
+        batch = dec + pre + new
 
         status = STATUS_OK
         if not batch and (stalled or self.waiting):
             status = STATUS_NO_BLOCKS
-        step = self._emit(batch, num_decodes, stalled, status)
+        step = self._emit(batch, len(dec), stalled, status)
         # an OK step (possibly empty) is committed by step_done; a NO_BLOCKS
         # step allocated nothing and leaves nothing to commit
         self._pending = batch if status == STATUS_OK else None

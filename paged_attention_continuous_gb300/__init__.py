@@ -59,7 +59,9 @@ class cb_config(ctypes.Structure):
                 ("max_prefill_chunk", ctypes.c_int32),
                 ("max_blocks_per_seq", ctypes.c_int32),
                 ("safety_margin", ctypes.c_float),
-                ("initial_free_list", ctypes.POINTER(ctypes.c_int32))]
+                ("initial_free_list", ctypes.POINTER(ctypes.c_int32)),
+                ("policy", ctypes.c_int32), ("max_prefill_reqs", ctypes.c_int32),
+                ("long_prefill_tokens", ctypes.c_int32), ("max_long_prefills", ctypes.c_int32)]
 
 
 class cb_step(ctypes.Structure):
@@ -139,16 +141,25 @@ def _arr(ptr, n, dtype):
     return np.ctypeslib.as_array(ptr, shape=(n,)).astype(dtype, copy=True)
 
 
+POLICY_FIFO, POLICY_PREFILL_FIRST = 0, 1
+
+
 class Scheduler:
-    """FIFO continuous-batching scheduler (C++), see ``cb_schedule_step``."""
+    """Continuous-batching scheduler (C++), see ``cb_schedule_step``:
+    policy FIFO (default) or PREFILL_FIRST, optional prefill-row and
+    long-prefill caps."""
 
     def __init__(self, *, block_size: int, num_blocks: int, max_batch_tokens: int,
                  max_requests_per_batch: int, max_blocks_per_seq: int,
                  max_prefill_chunk: int = 0, safety_margin: float = 0.15,
-                 free_list: Optional[Sequence[int]] = None):
+                 free_list: Optional[Sequence[int]] = None, policy: int = POLICY_FIFO,
+                 max_prefill_reqs: int = 0, long_prefill_tokens: int = 0,
+                 max_long_prefills: int = 1):
         self.max_blocks_per_seq = int(max_blocks_per_seq)
         cfg = cb_config(block_size, num_blocks, max_batch_tokens, max_requests_per_batch,
-                        max_prefill_chunk, max_blocks_per_seq, float(safety_margin), None)
+                        max_prefill_chunk, max_blocks_per_seq, float(safety_margin), None,
+                        int(policy), int(max_prefill_reqs), int(long_prefill_tokens),
+                        int(max_long_prefills))
         keep = None
         if free_list is not None:
             keep = np.ascontiguousarray(np.asarray(free_list, dtype=np.int32))

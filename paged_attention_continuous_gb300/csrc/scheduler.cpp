@@ -26,6 +26,15 @@
 // batch order and logical block order); the margin test is
 // free_after >= ceil((double)margin * num_blocks) for new requests only; the
 // step that completes a prompt yields the first output token.
+//
+// Policies: FIFO (above) or PrefillFirst ("Continuous batching architecture",
+// PrefillFirst: chunked prefills are completed before decoding resumes):
+// running prefills, then new prompts, then decodes with the budget and
+// request cap that are left; rows are still emitted decodes first.  Optional
+// caps: prefill rows per step, and (vLLM performance post, request-parallel
+// prefill) the number of long prompts in their prefill phase at once -- a
+// long waiting request held by that cap is skipped instead of blocking the
+// shorter requests behind it.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -159,8 +168,11 @@ cb_status cb_sched_create(const cb_config* cfg, cb_sched** out) {
   if (!cfg) return cb::fail(CB_ERR_INVALID_ARG, "cfg is NULL");
   if (cfg->block_size <= 0 || cfg->num_blocks <= 0 || cfg->max_batch_tokens <= 0 ||
       cfg->max_requests_per_batch <= 0 || cfg->max_blocks_per_seq <= 0 ||
-      cfg->max_prefill_chunk < 0)
+      cfg->max_prefill_chunk < 0 || cfg->max_prefill_reqs < 0 || cfg->long_prefill_tokens < 0 ||
+      cfg->max_long_prefills < 0)
     return cb::fail(CB_ERR_INVALID_ARG, "config sizes must be positive");
+  if (cfg->policy != CB_POLICY_FIFO && cfg->policy != CB_POLICY_PREFILL_FIRST)
+    return cb::fail(CB_ERR_INVALID_ARG, "unknown policy %d", cfg->policy);
   if (!(cfg->safety_margin >= 0.0f) || cfg->safety_margin > 1.0f)
     return cb::fail(CB_ERR_INVALID_ARG, "safety_margin must be in [0, 1]");
   std::unique_ptr<cb_sched> s(new (std::nothrow) cb_sched());
@@ -233,57 +245,94 @@ cb_status cb_schedule_step(cb_sched* s, cb_step* out) {
   int64_t budget = s->cfg.max_batch_tokens;
   const size_t cap = (size_t)s->cfg.max_requests_per_batch;
   const int64_t chunk_cap = s->cfg.max_prefill_chunk;
+  const size_t mpr = (size_t)s->cfg.max_prefill_reqs;
   s->batch.clear();
   s->stalled_ids.clear();
   s->stalled_demand.clear();
+  std::vector<cb::Scheduled> dec, pre, fresh;
+  auto rows = [&] { return dec.size() + pre.size() + fresh.size(); };
+  auto prefill_cap_hit = [&] { return mpr > 0 && pre.size() + fresh.size() >= mpr; };
+  auto is_long = [&](const cb::Request* r) {
+    return s->cfg.long_prefill_tokens > 0 && r->prompt_len > s->cfg.long_prefill_tokens;
+  };
+  auto stall = [&](const cb::Request* r, int64_t need) {
+    s->stalled_ids.push_back(r->id);
+    s->stalled_demand.push_back((int32_t)need);
+  };
 
-  // 1) running decodes, one token each
-  for (cb::Request* r : s->running) {
-    if (r->state != cb::State::kDecoding) continue;
-    if (budget == 0 || s->batch.size() == cap) break;
-    const int64_t need = blocks_for(s, (int64_t)r->num_cached + 1) - (int64_t)r->blocks.size();
-    if (need > (int64_t)s->free_list.size()) {
-      s->stalled_ids.push_back(r->id);
-      s->stalled_demand.push_back((int32_t)need);
-      continue;
+  // running decodes, one token each, admission order
+  auto decodes = [&] {
+    for (cb::Request* r : s->running) {
+      if (r->state != cb::State::kDecoding) continue;
+      if (budget == 0 || rows() == cap) break;
+      const int64_t need = blocks_for(s, (int64_t)r->num_cached + 1) - (int64_t)r->blocks.size();
+      if (need > (int64_t)s->free_list.size()) {
+        stall(r, need);
+        continue;
+      }
+      take_blocks(s, r, need);
+      dec.push_back({r, 1});
+      budget -= 1;
     }
-    take_blocks(s, r, need);
-    s->batch.push_back({r, 1});
-    budget -= 1;
-  }
-  const int32_t num_decodes = (int32_t)s->batch.size();
-
-  // 2) running prefills, next chunk each
-  for (cb::Request* r : s->running) {
-    if (r->state != cb::State::kPrefilling) continue;
-    if (budget == 0 || s->batch.size() == cap) break;
-    int64_t n = std::min<int64_t>(r->prompt_len - r->num_cached, budget);
-    if (chunk_cap > 0) n = std::min(n, chunk_cap);
-    const int64_t need = blocks_for(s, r->num_cached + n) - (int64_t)r->blocks.size();
-    if (need > (int64_t)s->free_list.size()) {
-      s->stalled_ids.push_back(r->id);
-      s->stalled_demand.push_back((int32_t)need);
-      continue;
+  };
+  // running prefills, next chunk each, admission order
+  auto running_prefills = [&] {
+    for (cb::Request* r : s->running) {
+      if (r->state != cb::State::kPrefilling) continue;
+      if (budget == 0 || rows() == cap || prefill_cap_hit()) break;
+      int64_t n = std::min<int64_t>(r->prompt_len - r->num_cached, budget);
+      if (chunk_cap > 0) n = std::min(n, chunk_cap);
+      const int64_t need = blocks_for(s, r->num_cached + n) - (int64_t)r->blocks.size();
+      if (need > (int64_t)s->free_list.size()) {
+        stall(r, need);
+        continue;
+      }
+      take_blocks(s, r, need);
+      pre.push_back({r, (int32_t)n});
+      budget -= n;
     }
-    take_blocks(s, r, need);
-    s->batch.push_back({r, (int32_t)n});
-    budget -= n;
-  }
+  };
+  // waiting requests, arrival order, head-of-line except long prompts held
+  // back by the long-prefill cap
+  auto admissions = [&] {
+    size_t i = 0;
+    while (i < s->waiting.size() && budget > 0 && rows() < cap && !prefill_cap_hit()) {
+      cb::Request* r = s->waiting[i];
+      if (is_long(r)) {
+        int32_t active = 0;
+        for (const cb::Request* x : s->running)
+          if (x->state == cb::State::kPrefilling && is_long(x)) ++active;
+        if (active >= s->cfg.max_long_prefills) {
+          ++i;
+          continue;
+        }
+      }
+      int64_t n = std::min<int64_t>(r->prompt_len, budget);
+      if (chunk_cap > 0) n = std::min(n, chunk_cap);
+      const int64_t need = blocks_for(s, n);
+      if ((int64_t)s->free_list.size() - need < s->reserved_blocks) break;
+      s->waiting.erase(s->waiting.begin() + (std::ptrdiff_t)i);
+      take_blocks(s, r, need);
+      r->state = cb::State::kPrefilling;
+      s->running.push_back(r);
+      fresh.push_back({r, (int32_t)n});
+      budget -= n;
+    }
+  };
 
-  // 3) waiting requests, arrival order, head-of-line
-  while (!s->waiting.empty() && budget > 0 && s->batch.size() < cap) {
-    cb::Request* r = s->waiting.front();
-    int64_t n = std::min<int64_t>(r->prompt_len, budget);
-    if (chunk_cap > 0) n = std::min(n, chunk_cap);
-    const int64_t need = blocks_for(s, n);
-    if ((int64_t)s->free_list.size() - need < s->reserved_blocks) break;
-    s->waiting.pop_front();
-    take_blocks(s, r, need);
-    r->state = cb::State::kPrefilling;
-    s->running.push_back(r);
-    s->batch.push_back({r, (int32_t)n});
-    budget -= n;
+  if (s->cfg.policy == CB_POLICY_PREFILL_FIRST) {
+    running_prefills();
+    admissions();
+    decodes();
+  } else {
+    decodes();
+    running_prefills();
+    admissions();
   }
+  const int32_t num_decodes = (int32_t)dec.size();
+  s->batch = dec;
+  s->batch.insert(s->batch.end(), pre.begin(), pre.end());
+  s->batch.insert(s->batch.end(), fresh.begin(), fresh.end());
 
   emit_step(s, num_decodes, out);
   if (s->batch.empty() && (!s->stalled_ids.empty() || !s->waiting.empty())) {

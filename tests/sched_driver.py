@@ -29,7 +29,10 @@ def oracle_from_config(cfg: dict):
                          max_blocks_per_seq=cfg["max_blocks_per_seq"],
                          max_prefill_chunk=cfg["max_prefill_chunk"],
                          safety_margin=cfg["safety_margin"],
-                         free_list=cfg.get("free_list"))
+                         free_list=cfg.get("free_list"), policy=cfg.get("policy", 0),
+                         max_prefill_reqs=cfg.get("max_prefill_reqs", 0),
+                         long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
+                         max_long_prefills=cfg.get("max_long_prefills", 1))
 
 
 def run_trace(sched, requests, num_steps, arrivals=None):

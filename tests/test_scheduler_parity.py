@@ -22,7 +22,10 @@ def c_from_config(cfg):
                         max_requests_per_batch=cfg["max_requests_per_batch"],
                         max_blocks_per_seq=cfg["max_blocks_per_seq"],
                         max_prefill_chunk=cfg["max_prefill_chunk"],
-                        safety_margin=cfg["safety_margin"], free_list=cfg.get("free_list"))
+                        safety_margin=cfg["safety_margin"], free_list=cfg.get("free_list"),
+                        policy=cfg.get("policy", 0), max_prefill_reqs=cfg.get("max_prefill_reqs", 0),
+                        long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
+                        max_long_prefills=cfg.get("max_long_prefills", 1))
 
 
 def _traces():

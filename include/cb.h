@@ -125,6 +125,24 @@ typedef struct cb_config {
                                      parallel prefill); a long waiting
                                      request held by it is skipped, not
                                      blocking shorter ones behind it */
+  int32_t offload;                /* 0: stalled requests are only reported.
+                                     1: offload them ("Continuous batching
+                                     architecture", Offloading / Soft
+                                     reset): the fewest stalled requests,
+                                     newest first, never the last active
+                                     one, when a batch was scheduled; when
+                                     none fits, the newest active requests,
+                                     retrying within the step.  A victim
+                                     goes to the CPU swap pool if its free
+                                     slots hold all its blocks, else it is
+                                     soft-reset (generated tokens join the
+                                     prompt, blocks freed, front of the
+                                     queue).  Swapped requests are resumed,
+                                     oldest offload first, at the start of a
+                                     later step when blocks allow. */
+  int32_t swap_blocks;            /* CPU swap pool capacity in blocks (one
+                                     block of every layer's K and V per
+                                     slot); 0 = soft reset only */
 } cb_config;
 
 #define CB_POLICY_FIFO 0
@@ -155,6 +173,16 @@ typedef struct cb_step {
                                     blocks they need this step */
   const int64_t* stalled_ids;    /* [num_stalled] */
   const int32_t* stalled_demand; /* [num_stalled] blocks each one needs */
+  /* KV copies the caller must make BEFORE this step's kernels, in this
+   * order (also when the step returns CB_ERR_NO_BLOCKS): swap-ins, swap
+   * pool slot -> cache block; then swap-outs, cache block -> swap pool
+   * slot (cb_kv_swap moves every layer's K and V of each pair). */
+  int32_t num_swap_in;
+  const int32_t* swap_in_slots;  /* [num_swap_in] */
+  const int32_t* swap_in_blocks; /* [num_swap_in] */
+  int32_t num_swap_out;
+  const int32_t* swap_out_blocks; /* [num_swap_out] */
+  const int32_t* swap_out_slots;  /* [num_swap_out] */
 } cb_step;
 
 /* Create / destroy a scheduler.  *out is NULL on failure. */
@@ -205,6 +233,11 @@ cb_status cb_sched_counts(const cb_sched* s, int32_t* free_blocks,
  * its length. */
 cb_status cb_sched_free_list(const cb_sched* s, int32_t* out, int32_t capacity,
                              int32_t* count);
+
+/* Requests currently in the swap pool (offload order) into out[0..capacity);
+ * *count gets their number; free swap slots into *free_slots (NULL ok). */
+cb_status cb_sched_swapped(const cb_sched* s, int64_t* out, int32_t capacity,
+                           int32_t* count, int32_t* free_slots);
 
 /* ------------------------------------------------------------------------
  * cb_kv_append (GPU).  "vLLM serving internals", PagedAttention as a virtual

@@ -28,6 +28,13 @@ Follows:
   remaining budget.
 * *Continuous batching architecture*, "PrefillFirst": chunked prefills are
   completed before decoding resumes (policy PREFILL_FIRST).
+* *Continuous batching architecture*, "Offloading" and "Soft reset": when
+  requests stall, the fewest of them are offloaded, newest first, never the
+  last active request -- to a CPU swap pool when it has room (resumed later
+  without recomputation), else by a soft reset (generated tokens appended
+  to the prompt, blocks freed, back to the queue).  Two triggers: a batch
+  was scheduled but requests stalled (offload enough stalled requests for
+  the rest); no batch fits at all (offload and retry within the step).
 * vLLM performance-series post (page 5), "Request-parallel prefill": several
   requests may prefill in one batch, but only a limited number of LONG
   prompts at a time, so short prompts are not held behind a long one.
@@ -68,6 +75,17 @@ Readings where the pages leave a step open:
    than ``max_long_prefills`` long requests are in their prefill phase, and
    one held by that cap is skipped (keeps its place) instead of blocking
    the requests behind it.
+11. Offloading (``offload=True``): swapped requests are resumed at the start
+   of a step, oldest offload first, head-of-line, when free blocks minus
+   their blocks stay >= the safety reserve; they rejoin the running list at
+   its end and are not chosen as victims in that step.  "Newest" = latest
+   in the running (admission) list.  A victim goes to the swap pool iff its
+   free slots hold all its blocks (slots from a FIFO queue, freed to its
+   tail); otherwise it is soft-reset: prompt_len += num_generated,
+   output_len -= num_generated, nothing cached, put at the FRONT of the
+   waiting queue.  Trigger 2 retries the whole schedule after each victim.
+   The step reports the copies to make before its kernels: swap-ins
+   (slot -> new block) first, then swap-outs (block -> slot).
 
 Parity: pinned by hand-derived traces (tests/golden/scheduler_*.json) and by
 invariants (budget, cap, FIFO order, block conservation, all-or-nothing
@@ -83,6 +101,7 @@ from typing import Dict, List, Optional, Sequence
 import numpy as np
 
 WAITING, PREFILLING, DECODING, FINISHED = "waiting", "prefilling", "decoding", "finished"
+SWAPPED = "swapped"
 
 STATUS_OK = 0
 STATUS_NO_BLOCKS = 2
@@ -98,6 +117,8 @@ class Request:
         self.num_generated = 0    # output tokens produced so far
         self.blocks: List[int] = []
         self.state = WAITING
+        self.swap_slots: List[int] = []
+        self.resume_state = None
 
 
 class FifoScheduler:
@@ -107,7 +128,8 @@ class FifoScheduler:
                  safety_margin: float = 0.15,
                  free_list: Optional[Sequence[int]] = None,
                  policy: int = POLICY_FIFO, max_prefill_reqs: int = 0,
-                 long_prefill_tokens: int = 0, max_long_prefills: int = 1):
+                 long_prefill_tokens: int = 0, max_long_prefills: int = 1,
+                 offload: bool = False, swap_blocks: int = 0):
         self.block_size = int(block_size)
         self.num_blocks = int(num_blocks)
         self.max_batch_tokens = int(max_batch_tokens)
@@ -118,6 +140,9 @@ class FifoScheduler:
         self.max_prefill_reqs = int(max_prefill_reqs)
         self.long_prefill_tokens = int(long_prefill_tokens)
         self.max_long_prefills = int(max_long_prefills)
+        self.offload = bool(offload)
+        self.swap_free = collections.deque(range(int(swap_blocks)))
+        self.swapped: List[Request] = []
         margin32 = float(np.float32(safety_margin))
         self.reserved_blocks = int(math.ceil(margin32 * float(self.num_blocks)))
         if free_list is None:
@@ -180,9 +205,9 @@ class FifoScheduler:
     def _is_long(self, r) -> bool:
         return self.long_prefill_tokens > 0 and r.prompt_len > self.long_prefill_tokens
 
-    def schedule_step(self) -> dict:
-        if self._pending is not None:
-            raise RuntimeError("schedule_step called twice without step_done")
+    def _schedule(self):
+        """One scheduling pass (no offloading); returns (batch, num_decodes,
+        stalled).  An empty batch has allocated nothing."""
         budget = self.max_batch_tokens
         cap = self.max_requests_per_batch
         mpr = self.max_prefill_reqs
@@ -263,11 +288,79 @@ class FifoScheduler:
             running_prefills()
             admissions()
         batch = dec + pre + new
+        return batch, len(dec), stalled
+
+    def _offload(self, r, swap_out) -> None:
+        """Take an active request off the GPU: to the swap pool if it has room
+        for all its blocks, else a soft reset."""
+        self.running.remove(r)
+        if self.swap_free and len(self.swap_free) >= len(r.blocks):
+            r.swap_slots = [self.swap_free.popleft() for _ in r.blocks]
+            swap_out.extend(zip(r.blocks, r.swap_slots))
+            r.resume_state = r.state
+            r.state = SWAPPED
+            self.swapped.append(r)
+        else:
+            r.prompt_len += r.num_generated
+            r.output_len -= r.num_generated
+            r.num_cached = 0
+            r.num_generated = 0
+            r.state = WAITING
+            self.waiting.appendleft(r)
+        for b in r.blocks:
+            self.free.append(b)
+        r.blocks = []
+
+    def schedule_step(self) -> dict:
+        if self._pending is not None:
+            raise RuntimeError("schedule_step called twice without step_done")
+        swap_in, swap_out = [], []     # (slot, block), (block, slot)
+        resumed = set()
+        if self.offload:
+            # resume swapped requests, oldest offload first, while blocks allow
+            while self.swapped:
+                r = self.swapped[0]
+                need = len(r.swap_slots)
+                if len(self.free) - need < self.reserved_blocks:
+                    break
+                del self.swapped[0]
+                for slot in r.swap_slots:
+                    b = self.free.popleft()
+                    r.blocks.append(b)
+                    swap_in.append((slot, b))
+                for slot in r.swap_slots:
+                    self.swap_free.append(slot)
+                r.swap_slots = []
+                r.state = r.resume_state
+                self.running.append(r)
+                resumed.add(r.req_id)
+        while True:
+            batch, nd, stalled = self._schedule()
+            if batch or not self.offload or not (stalled or self.waiting):
+                break
+            # nothing fits: offload the newest active request and retry
+            cands = [r for r in self.running if r.req_id not in resumed]
+            if len(self.running) <= 1 or not cands:
+                break
+            self._offload(cands[-1], swap_out)
+        if self.offload and batch and stalled:
+            # a batch fits but requests stalled: offload stalled requests,
+            # newest first, until the rest of the demand can be met
+            demand = {rid: need for rid, need in stalled}
+            order = [r for r in reversed(self.running)
+                     if r.req_id in demand and r.req_id not in resumed]
+            for r in order:
+                if len(self.free) >= sum(demand.values()) or len(self.running) <= 1:
+                    break
+                del demand[r.req_id]
+                self._offload(r, swap_out)
 
         status = STATUS_OK
         if not batch and (stalled or self.waiting):
             status = STATUS_NO_BLOCKS
-        step = self._emit(batch, len(dec), stalled, status)
+        step = self._emit(batch, nd, stalled, status)
+        step["swap_in"] = np.asarray(swap_in, dtype=np.int32).reshape(-1, 2)
+        step["swap_out"] = np.asarray(swap_out, dtype=np.int32).reshape(-1, 2)
         # an OK step (possibly empty) is committed by step_done; a NO_BLOCKS
         # step allocated nothing and leaves nothing to commit
         self._pending = batch if status == STATUS_OK else None
@@ -329,3 +422,6 @@ class FifoScheduler:
     # -------------------------------------------------------------- counts
     def counts(self):
         return len(self.free), len(self.waiting), len(self.running)
+
+    def swapped_ids(self) -> List[int]:
+        return [r.req_id for r in self.swapped]

@@ -61,7 +61,8 @@ class cb_config(ctypes.Structure):
                 ("safety_margin", ctypes.c_float),
                 ("initial_free_list", ctypes.POINTER(ctypes.c_int32)),
                 ("policy", ctypes.c_int32), ("max_prefill_reqs", ctypes.c_int32),
-                ("long_prefill_tokens", ctypes.c_int32), ("max_long_prefills", ctypes.c_int32)]
+                ("long_prefill_tokens", ctypes.c_int32), ("max_long_prefills", ctypes.c_int32),
+                ("offload", ctypes.c_int32), ("swap_blocks", ctypes.c_int32)]
 
 
 class cb_step(ctypes.Structure):
@@ -75,7 +76,13 @@ class cb_step(ctypes.Structure):
                 ("slot_mapping", ctypes.POINTER(ctypes.c_int32)),
                 ("num_stalled", ctypes.c_int32),
                 ("stalled_ids", ctypes.POINTER(ctypes.c_int64)),
-                ("stalled_demand", ctypes.POINTER(ctypes.c_int32))]
+                ("stalled_demand", ctypes.POINTER(ctypes.c_int32)),
+                ("num_swap_in", ctypes.c_int32),
+                ("swap_in_slots", ctypes.POINTER(ctypes.c_int32)),
+                ("swap_in_blocks", ctypes.POINTER(ctypes.c_int32)),
+                ("num_swap_out", ctypes.c_int32),
+                ("swap_out_blocks", ctypes.POINTER(ctypes.c_int32)),
+                ("swap_out_slots", ctypes.POINTER(ctypes.c_int32))]
 
 
 class cb_attention_args(ctypes.Structure):
@@ -109,6 +116,7 @@ def _declare():
     L.cb_request_slots.argtypes = [vp, i64, i32, i32, P(i32)]
     L.cb_sched_counts.argtypes = [vp, P(i32), P(i32), P(i32)]
     L.cb_sched_free_list.argtypes = [vp, P(i32), i32, P(i32)]
+    L.cb_sched_swapped.argtypes = [vp, P(ctypes.c_int64), i32, P(i32), P(i32)]
     L.cb_kv_append.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp]
     L.cb_attention_workspace_size.argtypes = [i32, i32, i32, i32]
     L.cb_attention_workspace_size.restype = sz
@@ -117,7 +125,8 @@ def _declare():
     L.cb_attention_read_errors.argtypes = [vp, sz, vp, P(ctypes.c_uint32)]
     for name in ("cb_sched_create", "cb_add_request", "cb_add_running_request",
                  "cb_schedule_step", "cb_step_done", "cb_request_slots", "cb_sched_counts",
-                 "cb_sched_free_list", "cb_kv_append", "cb_attention_workspace_init",
+                 "cb_sched_free_list", "cb_sched_swapped", "cb_kv_append",
+                 "cb_attention_workspace_init",
                  "cb_paged_attention", "cb_attention_read_errors"):
         getattr(L, name).restype = ctypes.c_int
 
@@ -154,12 +163,12 @@ class Scheduler:
                  max_prefill_chunk: int = 0, safety_margin: float = 0.15,
                  free_list: Optional[Sequence[int]] = None, policy: int = POLICY_FIFO,
                  max_prefill_reqs: int = 0, long_prefill_tokens: int = 0,
-                 max_long_prefills: int = 1):
+                 max_long_prefills: int = 1, offload: bool = False, swap_blocks: int = 0):
         self.max_blocks_per_seq = int(max_blocks_per_seq)
         cfg = cb_config(block_size, num_blocks, max_batch_tokens, max_requests_per_batch,
                         max_prefill_chunk, max_blocks_per_seq, float(safety_margin), None,
                         int(policy), int(max_prefill_reqs), int(long_prefill_tokens),
-                        int(max_long_prefills))
+                        int(max_long_prefills), int(bool(offload)), int(swap_blocks))
         keep = None
         if free_list is not None:
             keep = np.ascontiguousarray(np.asarray(free_list, dtype=np.int32))
@@ -203,7 +212,20 @@ class Scheduler:
             "slot_mapping": _arr(s.slot_mapping, T, np.int32),
             "stalled_ids": _arr(s.stalled_ids, s.num_stalled, np.int64),
             "stalled_demand": _arr(s.stalled_demand, s.num_stalled, np.int32),
+            "swap_in": np.stack([_arr(s.swap_in_slots, s.num_swap_in, np.int32),
+                                 _arr(s.swap_in_blocks, s.num_swap_in, np.int32)], axis=1),
+            "swap_out": np.stack([_arr(s.swap_out_blocks, s.num_swap_out, np.int32),
+                                  _arr(s.swap_out_slots, s.num_swap_out, np.int32)], axis=1),
         }
+
+    def swapped(self):
+        """(ids of requests in the swap pool in offload order, free slots)."""
+        n, f = ctypes.c_int32(), ctypes.c_int32()
+        _check(_lib.cb_sched_swapped(self._h, None, 0, ctypes.byref(n), ctypes.byref(f)))
+        out = np.zeros(max(n.value, 1), dtype=np.int64)
+        _check(_lib.cb_sched_swapped(self._h, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                     n.value, ctypes.byref(n), ctypes.byref(f)))
+        return [int(x) for x in out[:n.value]], f.value
 
     def step_done(self) -> list:
         n = ctypes.c_int32()

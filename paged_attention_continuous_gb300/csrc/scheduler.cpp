@@ -35,6 +35,18 @@
 // prefill) the number of long prompts in their prefill phase at once -- a
 // long waiting request held by that cap is skipped instead of blocking the
 // shorter requests behind it.
+//
+// Offloading ("Continuous batching architecture", Offloading and Soft
+// reset), when enabled: if a batch was scheduled but requests stalled, the
+// fewest stalled requests, newest first, are taken off the GPU until the
+// rest of the demand fits; if no batch fits at all, the newest active
+// request is taken off and the step is scheduled again, until one fits or
+// nothing is left to take.  The last active request is never taken.  A
+// victim goes to the CPU swap pool when its free slots hold all its blocks
+// (resumed later, oldest offload first, at the start of a step when blocks
+// allow, without recomputation), else it is soft-reset: its generated
+// tokens join its prompt, its blocks are freed and it goes to the front of
+// the waiting queue.  A request resumed in a step is not a victim in it.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -53,7 +65,7 @@ std::string& last_error_slot() {
   return s;
 }
 
-enum class State { kWaiting, kPrefilling, kDecoding, kFinished };
+enum class State { kWaiting, kPrefilling, kDecoding, kFinished, kSwapped };
 
 struct Request {
   int64_t id = 0;
@@ -63,6 +75,8 @@ struct Request {
   int32_t num_generated = 0;  // output tokens produced so far
   State state = State::kWaiting;
   std::vector<int32_t> blocks;
+  std::vector<int32_t> swap_slots;    // while swapped: slot of each block
+  State resume_state = State::kWaiting;
 };
 
 struct Scheduled {
@@ -87,6 +101,10 @@ struct cb_sched {
   std::vector<int64_t> stalled_ids;
   std::vector<int32_t> stalled_demand;
   std::vector<int64_t> finished_ids;
+  // offloading
+  std::deque<int32_t> swap_free;
+  std::vector<cb::Request*> swapped;  // offload order
+  std::vector<int32_t> swap_in_slots, swap_in_blocks, swap_out_blocks, swap_out_slots;
 };
 
 namespace {
@@ -152,96 +170,48 @@ void emit_step(cb_sched* s, int32_t num_decodes, cb_step* out) {
   out->num_stalled = (int32_t)s->stalled_ids.size();
   out->stalled_ids = s->stalled_ids.data();
   out->stalled_demand = s->stalled_demand.data();
+  out->num_swap_in = (int32_t)s->swap_in_slots.size();
+  out->swap_in_slots = s->swap_in_slots.data();
+  out->swap_in_blocks = s->swap_in_blocks.data();
+  out->num_swap_out = (int32_t)s->swap_out_blocks.size();
+  out->swap_out_blocks = s->swap_out_blocks.data();
+  out->swap_out_slots = s->swap_out_slots.data();
+}
+
+// Take an active request off the GPU: to the swap pool if its free slots
+// hold all its blocks, else a soft reset.
+void offload_request(cb_sched* s, cb::Request* r) {
+  s->running.erase(std::find(s->running.begin(), s->running.end(), r));
+  if (!s->swap_free.empty() && s->swap_free.size() >= r->blocks.size()) {
+    r->swap_slots.clear();
+    for (int32_t b : r->blocks) {
+      const int32_t slot = s->swap_free.front();
+      s->swap_free.pop_front();
+      r->swap_slots.push_back(slot);
+      s->swap_out_blocks.push_back(b);
+      s->swap_out_slots.push_back(slot);
+    }
+    r->resume_state = r->state;
+    r->state = cb::State::kSwapped;
+    s->swapped.push_back(r);
+  } else {
+    r->prompt_len += r->num_generated;
+    r->output_len -= r->num_generated;
+    r->num_cached = 0;
+    r->num_generated = 0;
+    r->state = cb::State::kWaiting;
+    s->waiting.push_front(r);
+  }
+  for (int32_t b : r->blocks) s->free_list.push_back(b);
+  r->blocks.clear();
 }
 
 }  // namespace
 
-extern "C" {
-
-const char* cb_last_error(void) { return cb::last_error_slot().c_str(); }
-
-int32_t cb_version(void) { return (1 << 16) | 0; }
-
-cb_status cb_sched_create(const cb_config* cfg, cb_sched** out) {
-  if (!out) return cb::fail(CB_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
-  if (!cfg) return cb::fail(CB_ERR_INVALID_ARG, "cfg is NULL");
-  if (cfg->block_size <= 0 || cfg->num_blocks <= 0 || cfg->max_batch_tokens <= 0 ||
-      cfg->max_requests_per_batch <= 0 || cfg->max_blocks_per_seq <= 0 ||
-      cfg->max_prefill_chunk < 0 || cfg->max_prefill_reqs < 0 || cfg->long_prefill_tokens < 0 ||
-      cfg->max_long_prefills < 0)
-    return cb::fail(CB_ERR_INVALID_ARG, "config sizes must be positive");
-  if (cfg->policy != CB_POLICY_FIFO && cfg->policy != CB_POLICY_PREFILL_FIRST)
-    return cb::fail(CB_ERR_INVALID_ARG, "unknown policy %d", cfg->policy);
-  if (!(cfg->safety_margin >= 0.0f) || cfg->safety_margin > 1.0f)
-    return cb::fail(CB_ERR_INVALID_ARG, "safety_margin must be in [0, 1]");
-  std::unique_ptr<cb_sched> s(new (std::nothrow) cb_sched());
-  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "out of host memory");
-  s->cfg = *cfg;
-  s->cfg.initial_free_list = nullptr;
-  s->reserved_blocks = (int64_t)std::ceil((double)cfg->safety_margin * (double)cfg->num_blocks);
-  if (cfg->initial_free_list) {
-    std::vector<char> seen(cfg->num_blocks, 0);
-    for (int32_t i = 0; i < cfg->num_blocks; ++i) {
-      const int32_t b = cfg->initial_free_list[i];
-      if (b < 0 || b >= cfg->num_blocks || seen[b])
-        return cb::fail(CB_ERR_INVALID_ARG, "initial_free_list is not a permutation");
-      seen[b] = 1;
-      s->free_list.push_back(b);
-    }
-  } else {
-    for (int32_t i = 0; i < cfg->num_blocks; ++i) s->free_list.push_back(i);
-  }
-  *out = s.release();
-  return CB_OK;
-}
-
-void cb_sched_destroy(cb_sched* s) { delete s; }
-
-cb_status cb_add_request(cb_sched* s, int64_t req_id, int32_t prompt_len, int32_t output_len) {
-  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
-  cb_status st = check_new_request(s, req_id, prompt_len, output_len);
-  if (st != CB_OK) return st;
-  auto r = std::make_unique<cb::Request>();
-  r->id = req_id;
-  r->prompt_len = prompt_len;
-  r->output_len = output_len;
-  s->waiting.push_back(r.get());
-  s->requests.emplace(req_id, std::move(r));
-  return CB_OK;
-}
-
-cb_status cb_add_running_request(cb_sched* s, int64_t req_id, int32_t prompt_len,
-                                 int32_t output_len, int32_t num_cached) {
-  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
-  cb_status st = check_new_request(s, req_id, prompt_len, output_len);
-  if (st != CB_OK) return st;
-  if (num_cached < 0 || (int64_t)num_cached > (int64_t)prompt_len + output_len - 2)
-    return cb::fail(CB_ERR_INVALID_ARG, "num_cached must be in [0, prompt_len + output_len - 2]");
-  if (s->step_open) return cb::fail(CB_ERR_STATE, "a step is open; call cb_step_done first");
-  const int64_t need = blocks_for(s, num_cached);
-  if (need > (int64_t)s->free_list.size())
-    return cb::fail(CB_ERR_NO_BLOCKS, "not enough free blocks to resume request %lld", (long long)req_id);
-  auto r = std::make_unique<cb::Request>();
-  r->id = req_id;
-  r->prompt_len = prompt_len;
-  r->output_len = output_len;
-  r->num_cached = num_cached;
-  if (num_cached >= prompt_len) {
-    r->state = cb::State::kDecoding;
-    r->num_generated = num_cached - prompt_len + 1;
-  } else {
-    r->state = cb::State::kPrefilling;
-  }
-  take_blocks(s, r.get(), need);
-  s->running.push_back(r.get());
-  s->requests.emplace(req_id, std::move(r));
-  return CB_OK;
-}
-
-cb_status cb_schedule_step(cb_sched* s, cb_step* out) {
-  if (!s || !out) return cb::fail(CB_ERR_INVALID_ARG, "NULL argument");
-  if (s->step_open) return cb::fail(CB_ERR_STATE, "previous step not committed with cb_step_done");
+namespace {
+// One scheduling pass without offloading: fills s->batch (rows decodes
+// first) and the stalled lists.  An empty batch has allocated nothing.
+void schedule_pass(cb_sched* s, int32_t* num_decodes) {
   int64_t budget = s->cfg.max_batch_tokens;
   const size_t cap = (size_t)s->cfg.max_requests_per_batch;
   const int64_t chunk_cap = s->cfg.max_prefill_chunk;
@@ -329,10 +299,174 @@ cb_status cb_schedule_step(cb_sched* s, cb_step* out) {
     running_prefills();
     admissions();
   }
-  const int32_t num_decodes = (int32_t)dec.size();
+  *num_decodes = (int32_t)dec.size();
   s->batch = dec;
   s->batch.insert(s->batch.end(), pre.begin(), pre.end());
   s->batch.insert(s->batch.end(), fresh.begin(), fresh.end());
+
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cb_last_error(void) { return cb::last_error_slot().c_str(); }
+
+int32_t cb_version(void) { return (1 << 16) | 0; }
+
+cb_status cb_sched_create(const cb_config* cfg, cb_sched** out) {
+  if (!out) return cb::fail(CB_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!cfg) return cb::fail(CB_ERR_INVALID_ARG, "cfg is NULL");
+  if (cfg->block_size <= 0 || cfg->num_blocks <= 0 || cfg->max_batch_tokens <= 0 ||
+      cfg->max_requests_per_batch <= 0 || cfg->max_blocks_per_seq <= 0 ||
+      cfg->max_prefill_chunk < 0 || cfg->max_prefill_reqs < 0 || cfg->long_prefill_tokens < 0 ||
+      cfg->max_long_prefills < 0 || cfg->swap_blocks < 0)
+    return cb::fail(CB_ERR_INVALID_ARG, "config sizes must be positive");
+  if (cfg->policy != CB_POLICY_FIFO && cfg->policy != CB_POLICY_PREFILL_FIRST)
+    return cb::fail(CB_ERR_INVALID_ARG, "unknown policy %d", cfg->policy);
+  if (!(cfg->safety_margin >= 0.0f) || cfg->safety_margin > 1.0f)
+    return cb::fail(CB_ERR_INVALID_ARG, "safety_margin must be in [0, 1]");
+  std::unique_ptr<cb_sched> s(new (std::nothrow) cb_sched());
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "out of host memory");
+  s->cfg = *cfg;
+  s->cfg.initial_free_list = nullptr;
+  s->reserved_blocks = (int64_t)std::ceil((double)cfg->safety_margin * (double)cfg->num_blocks);
+  for (int32_t i = 0; i < cfg->swap_blocks; ++i) s->swap_free.push_back(i);
+  if (cfg->initial_free_list) {
+    std::vector<char> seen(cfg->num_blocks, 0);
+    for (int32_t i = 0; i < cfg->num_blocks; ++i) {
+      const int32_t b = cfg->initial_free_list[i];
+      if (b < 0 || b >= cfg->num_blocks || seen[b])
+        return cb::fail(CB_ERR_INVALID_ARG, "initial_free_list is not a permutation");
+      seen[b] = 1;
+      s->free_list.push_back(b);
+    }
+  } else {
+    for (int32_t i = 0; i < cfg->num_blocks; ++i) s->free_list.push_back(i);
+  }
+  *out = s.release();
+  return CB_OK;
+}
+
+void cb_sched_destroy(cb_sched* s) { delete s; }
+
+cb_status cb_add_request(cb_sched* s, int64_t req_id, int32_t prompt_len, int32_t output_len) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  cb_status st = check_new_request(s, req_id, prompt_len, output_len);
+  if (st != CB_OK) return st;
+  auto r = std::make_unique<cb::Request>();
+  r->id = req_id;
+  r->prompt_len = prompt_len;
+  r->output_len = output_len;
+  s->waiting.push_back(r.get());
+  s->requests.emplace(req_id, std::move(r));
+  return CB_OK;
+}
+
+cb_status cb_add_running_request(cb_sched* s, int64_t req_id, int32_t prompt_len,
+                                 int32_t output_len, int32_t num_cached) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  cb_status st = check_new_request(s, req_id, prompt_len, output_len);
+  if (st != CB_OK) return st;
+  if (num_cached < 0 || (int64_t)num_cached > (int64_t)prompt_len + output_len - 2)
+    return cb::fail(CB_ERR_INVALID_ARG, "num_cached must be in [0, prompt_len + output_len - 2]");
+  if (s->step_open) return cb::fail(CB_ERR_STATE, "a step is open; call cb_step_done first");
+  const int64_t need = blocks_for(s, num_cached);
+  if (need > (int64_t)s->free_list.size())
+    return cb::fail(CB_ERR_NO_BLOCKS, "not enough free blocks to resume request %lld", (long long)req_id);
+  auto r = std::make_unique<cb::Request>();
+  r->id = req_id;
+  r->prompt_len = prompt_len;
+  r->output_len = output_len;
+  r->num_cached = num_cached;
+  if (num_cached >= prompt_len) {
+    r->state = cb::State::kDecoding;
+    r->num_generated = num_cached - prompt_len + 1;
+  } else {
+    r->state = cb::State::kPrefilling;
+  }
+  take_blocks(s, r.get(), need);
+  s->running.push_back(r.get());
+  s->requests.emplace(req_id, std::move(r));
+  return CB_OK;
+}
+
+cb_status cb_schedule_step(cb_sched* s, cb_step* out) {
+  if (!s || !out) return cb::fail(CB_ERR_INVALID_ARG, "NULL argument");
+  if (s->step_open) return cb::fail(CB_ERR_STATE, "previous step not committed with cb_step_done");
+  s->swap_in_slots.clear();
+  s->swap_in_blocks.clear();
+  s->swap_out_blocks.clear();
+  s->swap_out_slots.clear();
+  std::vector<cb::Request*> resumed;
+  const bool offload = s->cfg.offload != 0;
+  if (offload) {
+    // resume swapped requests, oldest offload first, while blocks allow
+    while (!s->swapped.empty()) {
+      cb::Request* r = s->swapped.front();
+      const int64_t need = (int64_t)r->swap_slots.size();
+      if ((int64_t)s->free_list.size() - need < s->reserved_blocks) break;
+      s->swapped.erase(s->swapped.begin());
+      for (int32_t slot : r->swap_slots) {
+        const int32_t b = s->free_list.front();
+        s->free_list.pop_front();
+        r->blocks.push_back(b);
+        s->swap_in_slots.push_back(slot);
+        s->swap_in_blocks.push_back(b);
+      }
+      for (int32_t slot : r->swap_slots) s->swap_free.push_back(slot);
+      r->swap_slots.clear();
+      r->state = r->resume_state;
+      s->running.push_back(r);
+      resumed.push_back(r);
+    }
+  }
+  auto was_resumed = [&](const cb::Request* r) {
+    return std::find(resumed.begin(), resumed.end(), r) != resumed.end();
+  };
+  int32_t num_decodes = 0;
+  while (true) {
+    schedule_pass(s, &num_decodes);
+    if (!s->batch.empty() || !offload || (s->stalled_ids.empty() && s->waiting.empty())) break;
+    // nothing fits: take the newest active request off and schedule again
+    cb::Request* victim = nullptr;
+    for (auto it = s->running.rbegin(); it != s->running.rend(); ++it)
+      if (!was_resumed(*it)) {
+        victim = *it;
+        break;
+      }
+    if (s->running.size() <= 1 || !victim) break;
+    offload_request(s, victim);
+  }
+  if (offload && !s->batch.empty() && !s->stalled_ids.empty()) {
+    // a batch fits but requests stalled: take stalled requests off, newest
+    // first, until the rest of the demand can be met
+    std::vector<std::pair<int64_t, int64_t>> demand;  // (id, blocks)
+    for (size_t i = 0; i < s->stalled_ids.size(); ++i)
+      demand.push_back({s->stalled_ids[i], s->stalled_demand[i]});
+    std::vector<cb::Request*> order;
+    for (auto it = s->running.rbegin(); it != s->running.rend(); ++it) {
+      const int64_t id = (*it)->id;
+      if (was_resumed(*it)) continue;
+      for (const auto& d : demand)
+        if (d.first == id) {
+          order.push_back(*it);
+          break;
+        }
+    }
+    for (cb::Request* r : order) {
+      int64_t total = 0;
+      for (const auto& d : demand) total += d.second;
+      if ((int64_t)s->free_list.size() >= total || s->running.size() <= 1) break;
+      for (size_t i = 0; i < demand.size(); ++i)
+        if (demand[i].first == r->id) {
+          demand.erase(demand.begin() + (std::ptrdiff_t)i);
+          break;
+        }
+      offload_request(s, r);
+    }
+  }
 
   emit_step(s, num_decodes, out);
   if (s->batch.empty() && (!s->stalled_ids.empty() || !s->waiting.empty())) {
@@ -401,6 +535,17 @@ cb_status cb_sched_counts(const cb_sched* s, int32_t* free_blocks, int32_t* num_
   if (free_blocks) *free_blocks = (int32_t)s->free_list.size();
   if (num_waiting) *num_waiting = (int32_t)s->waiting.size();
   if (num_running) *num_running = (int32_t)s->running.size();
+  return CB_OK;
+}
+
+cb_status cb_sched_swapped(const cb_sched* s, int64_t* out, int32_t capacity, int32_t* count,
+                           int32_t* free_slots) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  const int32_t n = (int32_t)s->swapped.size();
+  if (count) *count = n;
+  if (free_slots) *free_slots = (int32_t)s->swap_free.size();
+  if (out)
+    for (int32_t i = 0; i < std::min(n, capacity); ++i) out[i] = s->swapped[i]->id;
   return CB_OK;
 }
 

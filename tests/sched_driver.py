@@ -6,7 +6,7 @@ from __future__ import annotations
 import numpy as np
 
 FIELDS = ("status", "req_ids", "num_decodes", "cu_seqlens_q", "seq_lens",
-          "block_tables", "slot_mapping", "stalled_ids", "stalled_demand")
+          "block_tables", "slot_mapping", "stalled_ids", "stalled_demand", "swap_in", "swap_out")
 
 
 def normalize(step: dict) -> dict:
@@ -16,6 +16,8 @@ def normalize(step: dict) -> dict:
         if isinstance(v, np.ndarray):
             v = v.tolist()
         out[k] = v
+    for k in ("swap_in", "swap_out"):
+        out[k] = [list(map(int, p)) for p in out[k]]
     R = len(out["req_ids"])
     out["block_tables"] = [list(map(int, row)) for row in out["block_tables"]][:R]
     return out
@@ -32,7 +34,8 @@ def oracle_from_config(cfg: dict):
                          free_list=cfg.get("free_list"), policy=cfg.get("policy", 0),
                          max_prefill_reqs=cfg.get("max_prefill_reqs", 0),
                          long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
-                         max_long_prefills=cfg.get("max_long_prefills", 1))
+                         max_long_prefills=cfg.get("max_long_prefills", 1),
+                         offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0))
 
 
 def run_trace(sched, requests, num_steps, arrivals=None):

@@ -25,7 +25,8 @@ def c_from_config(cfg):
                         safety_margin=cfg["safety_margin"], free_list=cfg.get("free_list"),
                         policy=cfg.get("policy", 0), max_prefill_reqs=cfg.get("max_prefill_reqs", 0),
                         long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
-                        max_long_prefills=cfg.get("max_long_prefills", 1))
+                        max_long_prefills=cfg.get("max_long_prefills", 1),
+                        offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0))
 
 
 def _traces():

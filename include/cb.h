@@ -260,6 +260,37 @@ cb_status cb_kv_append(const void* k_new, const void* v_new,
                        uint32_t* error_word, cb_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * cb_kv_swap (GPU).  "Continuous batching architecture", Offloading: move
+ * whole KV blocks between two sets of pools in one launch -- for every pair
+ * i and every pool k:  dst_pools[k][dst_ids[i]] = src_pools[k][src_ids[i]]
+ * (block_bytes each).  The pools are typically every layer's K and V cache
+ * on one side and the same layers' pinned-host swap pools on the other;
+ * either side may be memory of the current device or pinned host memory
+ * (accessed directly by the kernel through its mapped device address);
+ * any other pointer is refused with CB_ERR_INVALID_ARG before a launch.  Pairs whose ids fall outside [0, src_capacity) /
+ * [0, dst_capacity) are skipped and flagged (CB_DEVERR_BLOCK_RANGE in
+ * error_word, optional).  src_ids/dst_ids are device arrays; the pool
+ * pointer arrays are host arrays read at the call.  The caller keeps the
+ * source blocks unchanged until the copy has run (stream order).
+ * ---------------------------------------------------------------------- */
+#define CB_SWAP_MAX_POOLS 128
+typedef struct cb_swap_args {
+  int32_t num_pairs;
+  const int32_t* src_ids;       /* device [num_pairs] */
+  const int32_t* dst_ids;       /* device [num_pairs] */
+  int32_t num_pools;            /* pools moved per pair, <= CB_SWAP_MAX_POOLS */
+  const void* const* src_pools; /* host [num_pools] base pointers, 16-B aligned */
+  void* const* dst_pools;       /* host [num_pools] base pointers, 16-B aligned */
+  int64_t src_capacity;         /* blocks in each source pool */
+  int64_t dst_capacity;         /* blocks in each destination pool */
+  int64_t block_bytes;          /* bytes per block (Hkv * block_size * D * elem),
+                                   a multiple of 16 */
+  uint32_t* error_word;         /* optional device word */
+} cb_swap_args;
+
+cb_status cb_kv_swap(const cb_swap_args* args, cb_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * cb_paged_attention (GPU).  "Chunked Prefill", How chunked prefill works:
  * query i of row r (absolute position p = seq_lens[r] - q_len + i) attends
  * to keys 0..p of its own request, read through block_tables[r]:

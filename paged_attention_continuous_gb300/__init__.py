@@ -100,6 +100,18 @@ class cb_attention_args(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t)]
 
 
+SWAP_MAX_POOLS = 128
+
+
+class cb_swap_args(ctypes.Structure):
+    _fields_ = [("num_pairs", ctypes.c_int32), ("src_ids", ctypes.c_void_p),
+                ("dst_ids", ctypes.c_void_p), ("num_pools", ctypes.c_int32),
+                ("src_pools", ctypes.POINTER(ctypes.c_void_p)),
+                ("dst_pools", ctypes.POINTER(ctypes.c_void_p)),
+                ("src_capacity", ctypes.c_int64), ("dst_capacity", ctypes.c_int64),
+                ("block_bytes", ctypes.c_int64), ("error_word", ctypes.c_void_p)]
+
+
 def _declare():
     L = _lib
     P = ctypes.POINTER
@@ -118,6 +130,7 @@ def _declare():
     L.cb_sched_free_list.argtypes = [vp, P(i32), i32, P(i32)]
     L.cb_sched_swapped.argtypes = [vp, P(ctypes.c_int64), i32, P(i32), P(i32)]
     L.cb_kv_append.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+    L.cb_kv_swap.argtypes = [P(cb_swap_args), vp]
     L.cb_attention_workspace_size.argtypes = [i32, i32, i32, i32]
     L.cb_attention_workspace_size.restype = sz
     L.cb_attention_workspace_init.argtypes = [vp, sz, vp]
@@ -125,7 +138,7 @@ def _declare():
     L.cb_attention_read_errors.argtypes = [vp, sz, vp, P(ctypes.c_uint32)]
     for name in ("cb_sched_create", "cb_add_request", "cb_add_running_request",
                  "cb_schedule_step", "cb_step_done", "cb_request_slots", "cb_sched_counts",
-                 "cb_sched_free_list", "cb_sched_swapped", "cb_kv_append",
+                 "cb_sched_free_list", "cb_sched_swapped", "cb_kv_append", "cb_kv_swap",
                  "cb_attention_workspace_init",
                  "cb_paged_attention", "cb_attention_read_errors"):
         getattr(L, name).restype = ctypes.c_int
@@ -297,6 +310,46 @@ def kv_append(k_new, v_new, slot_mapping, k_cache, v_cache, *, error_word=None,
                              _dtype_code(k_cache), ew, _stream_ptr(stream)))
 
 
+def kv_swap(src_pools, dst_pools, src_ids, dst_ids, *, error_word=None, stream=None) -> None:
+    """cb_kv_swap: for every pair i and pool k, block ``src_ids[i]`` of
+    ``src_pools[k]`` is copied to block ``dst_ids[i]`` of ``dst_pools[k]``.
+    Pools are contiguous tensors [capacity, ...] of one block shape, each on
+    the GPU or in pinned host memory; ids are int32 device tensors."""
+    if len(src_pools) != len(dst_pools):
+        raise ValueError("src_pools and dst_pools differ in length")
+    if len(src_pools) > SWAP_MAX_POOLS:
+        raise ValueError(f"at most {SWAP_MAX_POOLS} pools per call")
+    _need_cuda(src_ids, dst_ids)
+    n = int(src_ids.shape[0])
+    if int(dst_ids.shape[0]) != n:
+        raise ValueError("src_ids and dst_ids differ in length")
+    if n == 0 or not src_pools:
+        return
+    torch = _torch()
+    if src_ids.dtype != torch.int32 or dst_ids.dtype != torch.int32:
+        raise TypeError("ids must be int32")
+    blk = src_pools[0][0].numel() * src_pools[0].element_size()
+    for t in list(src_pools) + list(dst_pools):
+        if not t.is_contiguous():
+            raise ValueError("pools must be contiguous")
+        if not (t.is_cuda or t.is_pinned()):
+            raise ValueError("pools must live on the GPU or in pinned host memory")
+        if t[0].numel() * t.element_size() != blk:
+            raise ValueError("pools differ in block size")
+    for grp in (src_pools, dst_pools):
+        if len({int(t.shape[0]) for t in grp}) != 1:
+            raise ValueError("pools on one side differ in capacity")
+    P = ctypes.c_void_p * len(src_pools)
+    sp = P(*[t.data_ptr() for t in src_pools])
+    dp = P(*[t.data_ptr() for t in dst_pools])
+    a = cb_swap_args(n, src_ids.data_ptr(), dst_ids.data_ptr(), len(src_pools),
+                     ctypes.cast(sp, ctypes.POINTER(ctypes.c_void_p)),
+                     ctypes.cast(dp, ctypes.POINTER(ctypes.c_void_p)),
+                     int(src_pools[0].shape[0]), int(dst_pools[0].shape[0]), blk,
+                     error_word.data_ptr() if error_word is not None else None)
+    _check(_lib.cb_kv_swap(ctypes.byref(a), _stream_ptr(stream)))
+
+
 def workspace_size(num_reqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
     return int(_lib.cb_attention_workspace_size(num_reqs, num_q_heads, num_kv_heads, head_dim))
 
@@ -355,5 +408,5 @@ def paged_attention_args(**kw) -> cb_attention_args:
     return cb_attention_args(**kw)
 
 
-__all__ = ["Scheduler", "kv_append", "paged_attention", "Workspace", "workspace_size",
+__all__ = ["Scheduler", "kv_append", "kv_swap", "paged_attention", "Workspace", "workspace_size",
            "CBError", "version", "library", "LIB_PATH"]

@@ -7,7 +7,9 @@ forward pass.  This module is the attention part of that pass for one or
 more stacked layers: ``StepRunner.upload`` moves a step's host metadata
 (``cu_seqlens_q``, ``seq_lens``, ``block_tables``, ``slot_mapping``) to the
 device in ONE copy from pinned memory; ``StepRunner.run`` calls
-``cb_kv_append`` then ``cb_paged_attention`` on the current stream.
+``cb_kv_append`` then ``cb_paged_attention`` on the current stream.  With a
+swap pool (``swap_blocks``) the scheduler's offload swaps are queued ahead
+of each step (``SwapPool``).
 """
 from __future__ import annotations
 
@@ -17,7 +19,82 @@ from typing import Optional
 
 import numpy as np
 
-from . import Workspace, kv_append, paged_attention
+from . import SWAP_MAX_POOLS, Workspace, kv_append, kv_swap, paged_attention
+
+
+class SwapPool:
+    """Pinned host copies of offloaded requests' KV blocks.
+
+    "Continuous batching architecture", Offloading: an offloaded request's
+    blocks go to a preallocated pinned CPU pool and come back, without
+    recomputation, when GPU blocks free up.  The pool holds ``swap_blocks``
+    blocks per layer for K and for V, addressed by the scheduler's swap slot
+    ids.  ``apply(step)`` queues on the current stream the step's swap-ins
+    (slot -> cache block) and then its swap-outs (cache block -> slot), each
+    as cb_kv_swap calls over every layer's K and V; it must run before the
+    step's append and attention, and for every step the scheduler returns
+    (a step that found no blocks still carries swap pairs).  The two
+    directions are separate launches in that order because a slot a swap-in
+    frees may be refilled by a swap-out of the same step.
+    """
+
+    def __init__(self, k_cache, v_cache, swap_blocks: int, device="cuda"):
+        import torch
+        self.torch = torch
+        self.swap_blocks = int(swap_blocks)
+        shape = (self.swap_blocks,) + tuple(k_cache[0].shape[1:])
+        dt = k_cache[0].dtype
+        self.k = [torch.zeros(shape, dtype=dt, pin_memory=True) for _ in k_cache]
+        self.v = [torch.zeros(shape, dtype=dt, pin_memory=True) for _ in v_cache]
+        self._cache = list(k_cache) + list(v_cache)
+        self._pool = self.k + self.v
+        self.block_bytes = k_cache[0][0].numel() * k_cache[0].element_size()
+        cap = 4 * max(self.swap_blocks, 1)
+        self._host = [torch.empty(cap, dtype=torch.int32, pin_memory=True) for _ in range(2)]
+        self._copied = [None, None]
+        self._turn = 0
+        self._dev = torch.empty(cap, dtype=torch.int32, device=device)
+        self.error_word = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def apply(self, step: dict) -> int:
+        """Queue the step's swaps; returns the bytes moved over the CPU-GPU
+        link (both directions)."""
+        si = np.asarray(step.get("swap_in", np.zeros((0, 2))), dtype=np.int32).reshape(-1, 2)
+        so = np.asarray(step.get("swap_out", np.zeros((0, 2))), dtype=np.int32).reshape(-1, 2)
+        ni, no = len(si), len(so)
+        if ni + no == 0:
+            return 0
+        if ni > self.swap_blocks or no > self.swap_blocks:
+            raise ValueError("more swap pairs than swap slots")
+        b = self._turn
+        self._turn ^= 1
+        if self._copied[b] is not None:
+            self._copied[b].synchronize()
+        h = self._host[b].numpy()
+        h[0:ni] = si[:, 0]
+        h[ni:2 * ni] = si[:, 1]
+        h[2 * ni:2 * ni + no] = so[:, 0]
+        h[2 * ni + no:2 * ni + 2 * no] = so[:, 1]
+        n = 2 * (ni + no)
+        self._dev[:n].copy_(self._host[b][:n], non_blocking=True)
+        ev = self.torch.cuda.Event()
+        ev.record()
+        self._copied[b] = ev
+        d = self._dev
+        for lo in range(0, len(self._cache), SWAP_MAX_POOLS):
+            hi = lo + SWAP_MAX_POOLS
+            if ni:
+                kv_swap(self._pool[lo:hi], self._cache[lo:hi], d[0:ni], d[ni:2 * ni],
+                        error_word=self.error_word)
+        for lo in range(0, len(self._cache), SWAP_MAX_POOLS):
+            hi = lo + SWAP_MAX_POOLS
+            if no:
+                kv_swap(self._cache[lo:hi], self._pool[lo:hi], d[2 * ni:2 * ni + no],
+                        d[2 * ni + no:n], error_word=self.error_word)
+        return (ni + no) * len(self._cache) * self.block_bytes
+
+    def read_errors(self) -> int:
+        return int(self.error_word.item())
 
 
 @dataclasses.dataclass
@@ -38,7 +115,7 @@ class StepRunner:
     def __init__(self, *, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  dtype: str, max_reqs: int, max_tokens: int, max_blocks_per_seq: int,
                  num_layers: int = 1, block_size: int = 16, device: str = "cuda",
-                 scale: Optional[float] = None, zero_cache: bool = True):
+                 scale: Optional[float] = None, zero_cache: bool = True, swap_blocks: int = 0):
         import torch
         self.torch = torch
         self.dt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
@@ -53,6 +130,7 @@ class StepRunner:
         self.k_cache = [alloc(shape, dtype=self.dt, device=device) for _ in range(num_layers)]
         self.v_cache = [alloc(shape, dtype=self.dt, device=device) for _ in range(num_layers)]
         self.workspace = Workspace(max_reqs, num_q_heads, num_kv_heads, head_dim, device=device)
+        self.swap = SwapPool(self.k_cache, self.v_cache, swap_blocks, device) if swap_blocks else None
         cap = (max_reqs + 1) + max_reqs + max_reqs * max_blocks_per_seq + max_tokens
         # two pinned staging buffers, used in turn: a buffer is refilled only
         # after the copy that last read it has executed (its event), since
@@ -62,11 +140,22 @@ class StepRunner:
         self._turn = 0
         self._dev = torch.empty(cap, dtype=torch.int32, device=device)
 
+    def apply_swaps(self, step: dict) -> int:
+        """Queue the step's swap-ins and swap-outs (``SwapPool.apply``).
+        ``upload`` calls it; call it directly for a step that found no
+        blocks (it is not uploaded but may carry swap pairs)."""
+        if self.swap is None:
+            if len(step.get("swap_in", ())) or len(step.get("swap_out", ())):
+                raise ValueError("step carries swaps but the runner has no swap pool")
+            return 0
+        return self.swap.apply(step)
+
     def upload(self, step: dict, stream=None) -> DeviceStep:
-        """Copy a step's metadata to the device (one pinned copy on the
-        current stream).  The returned arrays stay valid until the next
-        upload on this runner; kernels that use them must be queued on the
-        same stream before that next upload."""
+        """Queue the step's swaps, then copy its metadata to the device (one
+        pinned copy on the current stream).  The returned arrays stay valid
+        until the next upload on this runner; kernels that use them must be
+        queued on the same stream before that next upload."""
+        self.apply_swaps(step)
         R, T = int(step["num_reqs"]), int(step["num_tokens"])
         if R > self.max_reqs or T > self.max_tokens:
             raise ValueError("step larger than the runner was sized for")
@@ -141,7 +230,7 @@ class GraphStepRunner:
     def __init__(self, *, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  dtype: str, max_reqs: int, max_tokens: int, max_blocks_per_seq: int,
                  num_layers: int = 1, block_size: int = 16, device: str = "cuda",
-                 scale: Optional[float] = None, zero_cache: bool = True):
+                 scale: Optional[float] = None, zero_cache: bool = True, swap_blocks: int = 0):
         import torch
         self.torch = torch
         self.dt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
@@ -157,6 +246,7 @@ class GraphStepRunner:
         self.k_cache = [alloc(shape, dtype=self.dt, device=device) for _ in range(num_layers)]
         self.v_cache = [alloc(shape, dtype=self.dt, device=device) for _ in range(num_layers)]
         self.workspace = Workspace(self.R_cap, num_q_heads, num_kv_heads, head_dim, device=device)
+        self.swap = SwapPool(self.k_cache, self.v_cache, swap_blocks, device) if swap_blocks else None
         mk = lambda h: [torch.zeros(self.T_cap, h, head_dim, dtype=self.dt, device=device)
                         for _ in range(num_layers)]
         self.q_buf, self.k_buf, self.v_buf = mk(num_q_heads), mk(num_kv_heads), mk(num_kv_heads)
@@ -169,8 +259,12 @@ class GraphStepRunner:
         self.graphs = {}
         self.pool = None
 
+    apply_swaps = StepRunner.apply_swaps
+
     def prepare(self, step: dict):
-        """Pad the step to its bucket and upload it; returns (key, T)."""
+        """Queue the step's swaps (uncaptured launches, ahead of the graph),
+        pad the step to its bucket and upload it; returns (key, T)."""
+        self.apply_swaps(step)
         R, T, nd = int(step["num_reqs"]), int(step["num_tokens"]), int(step["num_decodes"])
         npf = R - nd
         cu = np.asarray(step["cu_seqlens_q"], dtype=np.int64)
@@ -226,8 +320,11 @@ class GraphStepRunner:
         for layer in range(self.L):
             kc, vc = self.k_cache[layer], self.v_cache[layer]
             kv_append(self.k_buf[layer][:Tb], self.v_buf[layer][:Tb], sm, kc, vc)
+            # a chunk's bucket may pass the longest sequence the table spans;
+            # no real chunk does
             paged_attention(self.q_buf[layer][:Tb], kc, vc, cu, sl, bt, num_decodes=ndb,
-                            max_q_len=max(mqb, 1), max_seq_len=W * self.block_size,
+                            max_q_len=min(max(mqb, 1), W * self.block_size),
+                            max_seq_len=W * self.block_size,
                             scale=self.scale, workspace=self.workspace,
                             out=self.out_buf[layer][:Tb])
 

@@ -19,7 +19,8 @@ import torch
 import workloads
 from oracle import attention as oatt
 from oracle import paged_kv
-from tests.sched_driver import load_scenario, normalize, oracle_from_config, scenario_to_config
+from tests.sched_driver import (c_from_config, load_scenario, normalize, oracle_from_config,
+                                scenario_to_config)
 
 TOL = {"f32": (1e-4, 0.0), "bf16": (2e-2, 1e-2)}
 
@@ -43,12 +44,7 @@ class ParityRun:
         self.dtype = sc.dtype
         cfg = scenario_to_config(sc)
         self.o = oracle_from_config(cfg)
-        self.c = cb.Scheduler(block_size=cfg["block_size"], num_blocks=cfg["num_blocks"],
-                              max_batch_tokens=cfg["max_batch_tokens"],
-                              max_requests_per_batch=cfg["max_requests_per_batch"],
-                              max_blocks_per_seq=cfg["max_blocks_per_seq"],
-                              max_prefill_chunk=cfg["max_prefill_chunk"],
-                              safety_margin=cfg["safety_margin"], free_list=cfg["free_list"])
+        self.c = c_from_config(cfg)
         self.arrivals = arrivals
         self.next_arrival = 0
         if arrivals:
@@ -63,7 +59,8 @@ class ParityRun:
                                  dtype=sc.dtype, max_reqs=sc.max_requests_per_batch,
                                  max_tokens=max_tokens or sc.max_batch_tokens,
                                  max_blocks_per_seq=sc.max_blocks_per_seq,
-                                 num_layers=sc.num_layers, device=device)
+                                 num_layers=sc.num_layers, device=device,
+                                 swap_blocks=sc.swap_blocks)
         self.device = device
         self.pristine = []
         for layer in range(sc.num_layers):
@@ -82,6 +79,10 @@ class ParityRun:
         shape = (0, sc.num_kv_heads, sc.block_size, sc.head_dim)
         self.sub_k = [np.zeros(shape) for _ in range(sc.num_layers)]
         self.sub_v = [np.zeros(shape) for _ in range(sc.num_layers)]
+        # oracle swap pool: slot -> (k rows, v rows) per layer, or None when
+        # the block it came from was never followed
+        self.oswap = {}
+        self.swap_pairs = 0
         self.step_idx = 0
 
     def _followed(self, rid):
@@ -101,6 +102,25 @@ class ParityRun:
             self.sub_k[layer] = np.concatenate([self.sub_k[layer], k])
             self.sub_v[layer] = np.concatenate([self.sub_v[layer], v])
 
+    def _mirror_swaps(self, st):
+        """The oracle's side of a step's swaps, on its own sub-pool: swap-ins
+        (slot -> block) first, then swap-outs (block -> slot)."""
+        for slot, blk in st["swap_in"]:
+            got = self.oswap.pop(int(slot), None)
+            if got is None:
+                continue
+            self._snapshot([blk])
+            i = self.idx[int(blk)]
+            for layer, (k, v) in enumerate(got):
+                self.sub_k[layer][i] = k
+                self.sub_v[layer][i] = v
+        for blk, slot in st["swap_out"]:
+            i = self.idx.get(int(blk))
+            self.oswap[int(slot)] = None if i is None else [
+                (self.sub_k[layer][i].copy(), self.sub_v[layer][i].copy())
+                for layer in range(self.sc.num_layers)]
+        self.swap_pairs += len(st["swap_in"]) + len(st["swap_out"])
+
     def step(self):
         """One step on both sides.  Returns (status, gpu_out[layer] as float64
         numpy for followed rows, oracle_out[layer], followed token indices)."""
@@ -116,7 +136,9 @@ class ParityRun:
         sg = self.c.schedule_step()
         self.last = so
         assert normalize(so) == normalize(sg), "schedulers disagree"
+        self._mirror_swaps(so)
         if so["status"] != 0:
+            self.runner.apply_swaps(sg)
             self.step_idx += 1
             return so["status"], None, None, None
         T = so["num_tokens"]
@@ -164,5 +186,8 @@ class ParityRun:
         assert self.o.step_done() == self.c.step_done()
         errs = self.runner.workspace.read_errors()
         assert errs == 0, f"device error bits {errs:#x}"
+        if self.runner.swap is not None:
+            errs = self.runner.swap.read_errors()
+            assert errs == 0, f"swap error bits {errs:#x}"
         self.step_idx += 1
         return 0, gpu_outs, ref_outs, toks

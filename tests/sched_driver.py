@@ -66,7 +66,22 @@ def scenario_to_config(sc) -> dict:
             "max_prefill_chunk": sc.max_prefill_chunk,
             "safety_margin": sc.safety_margin,
             "max_blocks_per_seq": sc.max_blocks_per_seq,
-            "free_list": [int(x) for x in sc.free_list]}
+            "free_list": [int(x) for x in sc.free_list],
+            "policy": sc.policy, "offload": sc.offload, "swap_blocks": sc.swap_blocks}
+
+
+def c_from_config(cfg: dict):
+    import paged_attention_continuous_gb300 as cb
+    return cb.Scheduler(block_size=cfg["block_size"], num_blocks=cfg["num_blocks"],
+                        max_batch_tokens=cfg["max_batch_tokens"],
+                        max_requests_per_batch=cfg["max_requests_per_batch"],
+                        max_blocks_per_seq=cfg["max_blocks_per_seq"],
+                        max_prefill_chunk=cfg["max_prefill_chunk"],
+                        safety_margin=cfg["safety_margin"], free_list=cfg.get("free_list"),
+                        policy=cfg.get("policy", 0), max_prefill_reqs=cfg.get("max_prefill_reqs", 0),
+                        long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
+                        max_long_prefills=cfg.get("max_long_prefills", 1),
+                        offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0))
 
 
 def load_scenario(sched, sc, up_to_step=None):

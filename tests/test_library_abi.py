@@ -95,3 +95,31 @@ def test_scheduler_errors():
         s.schedule_step()               # previous step not committed
     assert e.value.status == cb.CB_ERR_STATE
     s.step_done()
+
+
+def test_kv_swap_argument_errors_without_gpu():
+    import paged_attention_continuous_gb300 as cb
+    lib = cb.library()
+    assert lib.cb_kv_swap(None, None) == cb.CB_ERR_INVALID_ARG
+    pools = (ctypes.c_void_p * 2)(256, 512)
+    P = ctypes.POINTER(ctypes.c_void_p)
+    pp = ctypes.cast(pools, P)
+    # nothing to move: accepted without touching the GPU
+    a = cb.cb_swap_args(0, None, None, 2, pp, pp, 4, 4, 4096, None)
+    assert lib.cb_kv_swap(ctypes.byref(a), None) == cb.CB_OK
+    a = cb.cb_swap_args(3, None, None, 0, None, None, 4, 4, 4096, None)
+    assert lib.cb_kv_swap(ctypes.byref(a), None) == cb.CB_OK
+    # too many pools, NULL ids, bad block size, bad capacity, misaligned pool
+    a = cb.cb_swap_args(1, 16, 16, cb.SWAP_MAX_POOLS + 1, pp, pp, 4, 4, 4096, None)
+    assert lib.cb_kv_swap(ctypes.byref(a), None) == cb.CB_ERR_INVALID_ARG
+    a = cb.cb_swap_args(1, None, 16, 2, pp, pp, 4, 4, 4096, None)
+    assert lib.cb_kv_swap(ctypes.byref(a), None) == cb.CB_ERR_INVALID_ARG
+    a = cb.cb_swap_args(1, 16, 16, 2, pp, pp, 4, 4, 4100, None)
+    assert lib.cb_kv_swap(ctypes.byref(a), None) == cb.CB_ERR_INVALID_ARG
+    assert "multiple of 16" in lib.cb_last_error().decode()
+    a = cb.cb_swap_args(1, 16, 16, 2, pp, pp, 0, 4, 4096, None)
+    assert lib.cb_kv_swap(ctypes.byref(a), None) == cb.CB_ERR_INVALID_ARG
+    bad = (ctypes.c_void_p * 2)(256, 520)
+    a = cb.cb_swap_args(1, 16, 16, 2, pp, ctypes.cast(bad, P), 4, 4, 4096, None)
+    assert lib.cb_kv_swap(ctypes.byref(a), None) == cb.CB_ERR_INVALID_ARG
+    assert "aligned" in lib.cb_last_error().decode()

@@ -111,3 +111,22 @@ def test_c_matches_oracle_random_pressure(seed):
     a = run_trace(oracle_from_config(cfg), reqs, 200)
     b = run_trace(c_from_config(cfg), reqs, 200)
     assert a == b
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_offload_pressure_workload_swaps_and_resets(seed):
+    """The GPU memory-pressure workload: every request finishes, blocks go
+    through the swap pool and some requests are soft-reset; the C++
+    scheduler agrees with the oracle on every step."""
+    import workloads
+    from tests.sched_driver import c_from_config, scenario_to_config
+    sc = workloads.offload_pressure(seed)
+    cfg = scenario_to_config(sc)
+    reqs = [dict(id=w.req_id, prompt_len=w.prompt_len, output_len=w.output_len,
+                 arrival_step=w.arrival_step) for w in sc.waiting]
+    o = oracle_from_config(cfg)
+    a = run_trace(o, reqs, 450)
+    assert a == run_trace(c_from_config(cfg), reqs, 450)
+    assert not o.running and not o.waiting and not o.swapped
+    assert sum(len(s["swap_out"]) for s in a) > 100
+    assert any(o.requests[r["id"]].prompt_len != r["prompt_len"] for r in reqs)

@@ -8,25 +8,11 @@ import numpy as np
 import pytest
 
 import workloads
-from tests.sched_driver import (load_scenario, normalize, oracle_from_config, run_trace,
-                                scenario_to_config)
+from tests.sched_driver import (c_from_config, load_scenario, normalize, oracle_from_config,
+                                run_trace, scenario_to_config)
 from tests.test_oracle_scheduler import _random_trace
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "scheduler_traces.json")
-
-
-def c_from_config(cfg):
-    import paged_attention_continuous_gb300 as cb
-    return cb.Scheduler(block_size=cfg["block_size"], num_blocks=cfg["num_blocks"],
-                        max_batch_tokens=cfg["max_batch_tokens"],
-                        max_requests_per_batch=cfg["max_requests_per_batch"],
-                        max_blocks_per_seq=cfg["max_blocks_per_seq"],
-                        max_prefill_chunk=cfg["max_prefill_chunk"],
-                        safety_margin=cfg["safety_margin"], free_list=cfg.get("free_list"),
-                        policy=cfg.get("policy", 0), max_prefill_reqs=cfg.get("max_prefill_reqs", 0),
-                        long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
-                        max_long_prefills=cfg.get("max_long_prefills", 1),
-                        offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0))
 
 
 def _traces():

@@ -78,6 +78,9 @@ class Scenario:
     value_scale: float = 1.0         # q/k/v ~ value_scale * N(0, 1)
     seed: int = 0
     block_size: int = BLOCK_SIZE
+    policy: int = 0                  # 0 FIFO, 1 PrefillFirst
+    offload: bool = False            # offload requests when blocks run out
+    swap_blocks: int = 0             # CPU swap pool capacity in blocks
 
     def __post_init__(self):
         longest = max([r.prompt_len + r.output_len - 1 for r in self.running]
@@ -216,6 +219,30 @@ def prefill_chunk_16k(seed: int = 0, chunk: int = 512, offset: int = 16384,
         running=running, waiting=[], value_scale=0.5, seed=seed)
 
 
+def offload_pressure(seed: int = 0, num_requests: int = 24, num_blocks: int = 40,
+                     swap_blocks: int = 8, num_layers: int = 2) -> Scenario:
+    """A KV pool too small for the requests it admits, with offloading on:
+    requests arrive over the first steps (prompts 24-160, outputs 16-96
+    tokens), the pool holds 640 tokens, so decodes outgrow it and requests
+    are moved to an 8-block CPU swap pool, or soft-reset when it is full, and
+    later resumed (seeds 0-3: 160-560 block swaps and 6-9 soft resets over
+    about 350 steps).  Each request alone fits the pool."""
+    rng = np.random.default_rng(seed)
+    waiting = []
+    for i in range(num_requests):
+        waiting.append(WaitingRequest(req_id=i, prompt_len=int(rng.integers(24, 160, endpoint=True)),
+                                      output_len=int(rng.integers(16, 96, endpoint=True)),
+                                      arrival_step=int(rng.integers(0, 12))))
+    waiting.sort(key=lambda w: w.arrival_step)
+    return Scenario(
+        name="offload_pressure", num_q_heads=16, num_kv_heads=4, head_dim=128,
+        dtype="bf16", num_blocks=num_blocks, max_batch_tokens=256,
+        max_requests_per_batch=16, max_prefill_chunk=0, safety_margin=0.0,
+        max_blocks_per_seq=0, free_list=permuted_free_list(num_blocks, seed + 1),
+        running=[], waiting=waiting, num_layers=num_layers, value_scale=1.0, seed=seed,
+        offload=True, swap_blocks=swap_blocks)
+
+
 SCENARIOS = {
     "chunked_prefill_1000": chunked_prefill_1000,
     "decode_64": decode_64,
@@ -223,6 +250,7 @@ SCENARIOS = {
     "long_prompt_32k": long_prompt_32k,
     "trace_2000": trace_2000,
     "prefill_chunk_16k": prefill_chunk_16k,
+    "offload_pressure": offload_pressure,
 }
 
 

@@ -143,6 +143,29 @@ typedef struct cb_config {
   int32_t swap_blocks;            /* CPU swap pool capacity in blocks (one
                                      block of every layer's K and V per
                                      slot); 0 = soft reset only */
+  int32_t prefix_caching;         /* 1: share blocks of equal prompt
+                                     prefixes ("Continuous batching
+                                     architecture", Prefix caching,
+                                     Eviction) among requests queued with
+                                     cb_add_request_tokens.  A block inside
+                                     the known prompt tokens is keyed, when
+                                     the step that completes it is
+                                     committed, by a fingerprint of the whole
+                                     token prefix up to its end (128 bits,
+                                     plus a check of the block's own tokens)
+                                     unless another block holds that key.
+                                     At admission the longest leading run of
+                                     keyed blocks is reused (at most
+                                     prompt_len - 1 tokens: one prompt token
+                                     is always computed); reused tokens are
+                                     cached and take no budget.  Blocks are
+                                     reference-counted; a freed keyed block
+                                     keeps its K/V and key in an
+                                     "initialized" pool and can still be
+                                     matched; allocation takes the free
+                                     queue first and then demotes the NEWEST
+                                     initialized block (its key dropped).
+                                     Free capacity counts both. */
 } cb_config;
 
 #define CB_POLICY_FIFO 0
@@ -195,6 +218,13 @@ void cb_sched_destroy(cb_sched* s);
 cb_status cb_add_request(cb_sched* s, int64_t req_id, int32_t prompt_len,
                          int32_t output_len);
 
+/* cb_add_request with the ids of the first num_tokens (<= prompt_len)
+ * prompt tokens (host array, copied), which prefix caching matches on.
+ * Without prefix_caching the ids are ignored. */
+cb_status cb_add_request_tokens(cb_sched* s, int64_t req_id, int32_t prompt_len,
+                                int32_t output_len, const int32_t* tokens,
+                                int32_t num_tokens);
+
 /* Resume a request whose first num_cached tokens already have K/V in the
  * cache (the swap-in path of "Offloading": resume without recomputing).  It
  * joins the running set after the requests already there and takes
@@ -215,7 +245,9 @@ cb_status cb_schedule_step(cb_sched* s, cb_step* out);
 
 /* Commit the last CB_OK step.  *num_finished / *finished_ids (host, owned by
  * the scheduler, valid until the next call) list requests that finished, in
- * batch order; their blocks went back to the tail of the free list.  Either
+ * batch order; their blocks went back to the tail of the free list (keyed
+ * blocks to the initialized pool, shared blocks once their last user
+ * finished).  Either
  * output pointer may be NULL. */
 cb_status cb_step_done(cb_sched* s, int32_t* num_finished,
                        const int64_t** finished_ids);
@@ -229,10 +261,17 @@ cb_status cb_request_slots(const cb_sched* s, int64_t req_id, int32_t start,
 cb_status cb_sched_counts(const cb_sched* s, int32_t* free_blocks,
                           int32_t* num_waiting, int32_t* num_running);
 
-/* Copies the free list (allocation order) into out[0..capacity); *count gets
- * its length. */
+/* Copies the free list into out[0..capacity): the free queue in allocation
+ * order, then the initialized pool (prefix caching) oldest first; *count
+ * gets its length. */
 cb_status cb_sched_free_list(const cb_sched* s, int32_t* out, int32_t capacity,
                              int32_t* count);
+
+/* Prefix caching counters (any pointer may be NULL): prompt tokens reused
+ * from cached blocks so far, keyed blocks, keyed blocks in the initialized
+ * pool (free but still matchable). */
+cb_status cb_sched_prefix_stats(const cb_sched* s, int64_t* hit_tokens,
+                                int32_t* keyed_blocks, int32_t* pool_blocks);
 
 /* Requests currently in the swap pool (offload order) into out[0..capacity);
  * *count gets their number; free swap slots into *free_slots (NULL ok). */

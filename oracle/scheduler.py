@@ -35,6 +35,13 @@ Follows:
   to the prompt, blocks freed, back to the queue).  Two triggers: a batch
   was scheduled but requests stalled (offload enough stalled requests for
   the rest); no batch fits at all (offload and retry within the step).
+* *Continuous batching architecture*, "Prefix caching" and "Eviction": a
+  content key per complete block; a later request whose prompt starts with
+  the same blocks reuses them and skips their prefill; shared blocks are
+  reference-counted and return to the pool when the last user finishes;
+  freed blocks keep their content and key ("initialized") so later requests
+  can still match them, and when uninitialized blocks run out the newest
+  initialized ones are demoted (key dropped) and reused.
 * vLLM performance-series post (page 5), "Request-parallel prefill": several
   requests may prefill in one batch, but only a limited number of LONG
   prompts at a time, so short prompts are not held behind a long one.
@@ -86,6 +93,22 @@ Readings where the pages leave a step open:
    waiting queue.  Trigger 2 retries the whole schedule after each victim.
    The step reports the copies to make before its kernels: swap-ins
    (slot -> new block) first, then swap-outs (block -> slot).
+12. Prefix caching (``prefix_caching=True``; only requests given prompt
+   token ids take part): a block's key is the whole token prefix up to its
+   end (so a block matches only after every block before it matched), for
+   blocks fully inside the known prompt tokens.  At admission the longest
+   leading run of cached keys is reused, capped so at least one prompt token
+   is computed (the step that completes the prompt yields the first output
+   token); the reused tokens count as cached and take no budget.  Reused
+   blocks with no other user leave the free pool, so admission needs
+   free - reused_free - new >= reserve.  A block is keyed at the step_done
+   that completes it, unless its key is already held by another block.  A
+   freed block whose count drops to 0 goes to the initialized pool (freed
+   order) if keyed, else to the tail of the free queue.  Allocation pops the
+   free queue; when it is empty it demotes the NEWEST initialized block.
+   Free capacity = free queue + initialized pool.  Offloaded or reset
+   requests release their blocks the same way; blocks swapped back in are
+   new private blocks.
 
 Parity: pinned by hand-derived traces (tests/golden/scheduler_*.json) and by
 invariants (budget, cap, FIFO order, block conservation, all-or-nothing
@@ -119,6 +142,8 @@ class Request:
         self.state = WAITING
         self.swap_slots: List[int] = []
         self.resume_state = None
+        self.tokens = None        # known prompt token ids (prefix caching)
+        self.num_registered = 0   # leading blocks already considered for keys
 
 
 class FifoScheduler:
@@ -129,7 +154,8 @@ class FifoScheduler:
                  free_list: Optional[Sequence[int]] = None,
                  policy: int = POLICY_FIFO, max_prefill_reqs: int = 0,
                  long_prefill_tokens: int = 0, max_long_prefills: int = 1,
-                 offload: bool = False, swap_blocks: int = 0):
+                 offload: bool = False, swap_blocks: int = 0,
+                 prefix_caching: bool = False):
         self.block_size = int(block_size)
         self.num_blocks = int(num_blocks)
         self.max_batch_tokens = int(max_batch_tokens)
@@ -148,6 +174,14 @@ class FifoScheduler:
         if free_list is None:
             free_list = range(self.num_blocks)
         self.free = collections.deque(int(b) for b in free_list)
+        # prefix caching: reference counts of blocks in use, keyed blocks
+        # (key = token prefix up to the block's end) and the initialized pool
+        self.prefix_caching = bool(prefix_caching)
+        self.refs: Dict[int, int] = {}
+        self.cache_index: Dict[tuple, int] = {}
+        self.block_key: Dict[int, tuple] = {}
+        self.free_init: List[int] = []
+        self.prefix_hit_tokens = 0
         self.waiting: collections.deque = collections.deque()
         self.running: List[Request] = []
         self.requests: Dict[int, Request] = {}
@@ -157,14 +191,64 @@ class FifoScheduler:
     def _blocks_for(self, num_tokens: int) -> int:
         return -(-num_tokens // self.block_size)
 
-    def add_request(self, req_id: int, prompt_len: int, output_len: int) -> None:
+    def add_request(self, req_id: int, prompt_len: int, output_len: int,
+                    tokens: Optional[Sequence[int]] = None) -> None:
+        """``tokens``: ids of the first len(tokens) <= prompt_len prompt
+        tokens (for prefix caching), or None."""
         if req_id in self.requests or prompt_len < 1 or output_len < 1:
             raise ValueError("bad request")
         if self._blocks_for(prompt_len + output_len - 1) > self.max_blocks_per_seq:
             raise ValueError("request longer than max_blocks_per_seq blocks")
+        if tokens is not None and len(tokens) > prompt_len:
+            raise ValueError("more tokens than prompt_len")
         r = Request(req_id, prompt_len, output_len)
+        if tokens is not None:
+            r.tokens = tuple(int(t) for t in tokens)
         self.requests[r.req_id] = r
         self.waiting.append(r)
+
+    # ------------------------------------------------------- block pool
+    def _num_free(self) -> int:
+        return len(self.free) + len(self.free_init)
+
+    def _alloc(self) -> int:
+        if self.free:
+            b = self.free.popleft()
+        else:
+            b = self.free_init.pop()          # demote the newest initialized block
+            del self.cache_index[self.block_key.pop(b)]
+        self.refs[b] = 1
+        return b
+
+    def _release(self, r) -> None:
+        for b in r.blocks:
+            self.refs[b] -= 1
+            if self.refs[b] == 0:
+                del self.refs[b]
+                if b in self.block_key:
+                    self.free_init.append(b)
+                else:
+                    self.free.append(b)
+        r.blocks = []
+        r.num_registered = 0
+
+    def _match(self, r) -> List[int]:
+        """Blocks of the longest leading run of r's prompt already cached."""
+        if not self.prefix_caching or r.tokens is None:
+            return []
+        limit = min(len(r.tokens), r.prompt_len - 1)
+        bs = self.block_size
+        out: List[int] = []
+        while (len(out) + 1) * bs <= limit:
+            b = self.cache_index.get(r.tokens[:(len(out) + 1) * bs])
+            if b is None:
+                break
+            out.append(b)
+        return out
+
+    def free_list(self) -> List[int]:
+        """Allocatable blocks: the free queue, then the initialized pool."""
+        return list(self.free) + list(self.free_init)
 
     def add_running_request(self, req_id: int, prompt_len: int,
                             output_len: int, num_cached: int) -> None:
@@ -179,7 +263,7 @@ class FifoScheduler:
         if self._blocks_for(prompt_len + output_len - 1) > self.max_blocks_per_seq:
             raise ValueError("request longer than max_blocks_per_seq blocks")
         need = self._blocks_for(num_cached)
-        if need > len(self.free):
+        if need > self._num_free():
             raise MemoryError("not enough free blocks")
         r = Request(req_id, prompt_len, output_len)
         r.num_cached = num_cached
@@ -189,7 +273,7 @@ class FifoScheduler:
         else:
             r.state = PREFILLING
         for _ in range(need):
-            r.blocks.append(self.free.popleft())
+            r.blocks.append(self._alloc())
         self.requests[r.req_id] = r
         self.running.append(r)
 
@@ -225,11 +309,11 @@ class FifoScheduler:
                 if budget == 0 or rows() == cap:
                     break
                 need = self._blocks_for(r.num_cached + 1) - len(r.blocks)
-                if need > len(self.free):
+                if need > self._num_free():
                     stalled.append((r.req_id, need))
                     continue
                 for _ in range(need):
-                    r.blocks.append(self.free.popleft())
+                    r.blocks.append(self._alloc())
                 dec.append((r, 1))
                 budget -= 1
 
@@ -245,11 +329,11 @@ class FifoScheduler:
                 if self.max_prefill_chunk > 0:
                     n = min(n, self.max_prefill_chunk)
                 need = self._blocks_for(r.num_cached + n) - len(r.blocks)
-                if need > len(self.free):
+                if need > self._num_free():
                     stalled.append((r.req_id, need))
                     continue
                 for _ in range(need):
-                    r.blocks.append(self.free.popleft())
+                    r.blocks.append(self._alloc())
                 pre.append((r, n))
                 budget -= n
 
@@ -265,15 +349,28 @@ class FifoScheduler:
                     if active >= self.max_long_prefills:
                         i += 1
                         continue
-                n = min(r.prompt_len, budget)
+                shared = self._match(r)
+                m = len(shared) * self.block_size
+                n = min(r.prompt_len - m, budget)
                 if self.max_prefill_chunk > 0:
                     n = min(n, self.max_prefill_chunk)
-                need = self._blocks_for(n)
-                if len(self.free) - need < self.reserved_blocks:
+                need = self._blocks_for(m + n) - len(shared)
+                from_pool = sum(1 for b in shared if b not in self.refs)
+                if self._num_free() - from_pool - need < self.reserved_blocks:
                     break
                 del self.waiting[i]
+                for b in shared:
+                    if b in self.refs:
+                        self.refs[b] += 1
+                    else:
+                        self.free_init.remove(b)
+                        self.refs[b] = 1
+                r.blocks = list(shared)
+                r.num_cached = m
+                r.num_registered = len(shared)
+                self.prefix_hit_tokens += m
                 for _ in range(need):
-                    r.blocks.append(self.free.popleft())
+                    r.blocks.append(self._alloc())
                 r.state = PREFILLING
                 self.running.append(r)
                 new.append((r, n))
@@ -307,9 +404,7 @@ class FifoScheduler:
             r.num_generated = 0
             r.state = WAITING
             self.waiting.appendleft(r)
-        for b in r.blocks:
-            self.free.append(b)
-        r.blocks = []
+        self._release(r)
 
     def schedule_step(self) -> dict:
         if self._pending is not None:
@@ -321,11 +416,11 @@ class FifoScheduler:
             while self.swapped:
                 r = self.swapped[0]
                 need = len(r.swap_slots)
-                if len(self.free) - need < self.reserved_blocks:
+                if self._num_free() - need < self.reserved_blocks:
                     break
                 del self.swapped[0]
                 for slot in r.swap_slots:
-                    b = self.free.popleft()
+                    b = self._alloc()
                     r.blocks.append(b)
                     swap_in.append((slot, b))
                 for slot in r.swap_slots:
@@ -350,7 +445,7 @@ class FifoScheduler:
             order = [r for r in reversed(self.running)
                      if r.req_id in demand and r.req_id not in resumed]
             for r in order:
-                if len(self.free) >= sum(demand.values()) or len(self.running) <= 1:
+                if self._num_free() >= sum(demand.values()) or len(self.running) <= 1:
                     break
                 del demand[r.req_id]
                 self._offload(r, swap_out)
@@ -411,17 +506,29 @@ class FifoScheduler:
             if r.state == DECODING and r.num_generated >= r.output_len:
                 r.state = FINISHED
                 finished.append(r)
+        if self.prefix_caching:
+            # key every block this step completed inside the known tokens
+            bs = self.block_size
+            for r, _ in self._pending:
+                if r.tokens is None:
+                    continue
+                full = min(r.num_cached, len(r.tokens)) // bs
+                while r.num_registered < full:
+                    i = r.num_registered
+                    key = r.tokens[:(i + 1) * bs]
+                    if key not in self.cache_index:
+                        self.cache_index[key] = r.blocks[i]
+                        self.block_key[r.blocks[i]] = key
+                    r.num_registered += 1
         for r in finished:
             self.running.remove(r)
-            for b in r.blocks:
-                self.free.append(b)
-            r.blocks = []
+            self._release(r)
         self._pending = None
         return [r.req_id for r in finished]
 
     # -------------------------------------------------------------- counts
     def counts(self):
-        return len(self.free), len(self.waiting), len(self.running)
+        return self._num_free(), len(self.waiting), len(self.running)
 
     def swapped_ids(self) -> List[int]:
         return [r.req_id for r in self.swapped]

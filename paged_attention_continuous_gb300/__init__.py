@@ -62,7 +62,8 @@ class cb_config(ctypes.Structure):
                 ("initial_free_list", ctypes.POINTER(ctypes.c_int32)),
                 ("policy", ctypes.c_int32), ("max_prefill_reqs", ctypes.c_int32),
                 ("long_prefill_tokens", ctypes.c_int32), ("max_long_prefills", ctypes.c_int32),
-                ("offload", ctypes.c_int32), ("swap_blocks", ctypes.c_int32)]
+                ("offload", ctypes.c_int32), ("swap_blocks", ctypes.c_int32),
+                ("prefix_caching", ctypes.c_int32)]
 
 
 class cb_step(ctypes.Structure):
@@ -122,6 +123,8 @@ def _declare():
     L.cb_sched_destroy.argtypes = [vp]
     L.cb_sched_destroy.restype = None
     L.cb_add_request.argtypes = [vp, i64, i32, i32]
+    L.cb_add_request_tokens.argtypes = [vp, i64, i32, i32, P(i32), i32]
+    L.cb_sched_prefix_stats.argtypes = [vp, P(i64), P(i32), P(i32)]
     L.cb_add_running_request.argtypes = [vp, i64, i32, i32, i32]
     L.cb_schedule_step.argtypes = [vp, P(cb_step)]
     L.cb_step_done.argtypes = [vp, P(i32), P(P(i64))]
@@ -136,7 +139,8 @@ def _declare():
     L.cb_attention_workspace_init.argtypes = [vp, sz, vp]
     L.cb_paged_attention.argtypes = [P(cb_attention_args), vp]
     L.cb_attention_read_errors.argtypes = [vp, sz, vp, P(ctypes.c_uint32)]
-    for name in ("cb_sched_create", "cb_add_request", "cb_add_running_request",
+    for name in ("cb_sched_create", "cb_add_request", "cb_add_request_tokens",
+                 "cb_sched_prefix_stats", "cb_add_running_request",
                  "cb_schedule_step", "cb_step_done", "cb_request_slots", "cb_sched_counts",
                  "cb_sched_free_list", "cb_sched_swapped", "cb_kv_append", "cb_kv_swap",
                  "cb_attention_workspace_init",
@@ -169,19 +173,21 @@ POLICY_FIFO, POLICY_PREFILL_FIRST = 0, 1
 class Scheduler:
     """Continuous-batching scheduler (C++), see ``cb_schedule_step``:
     policy FIFO (default) or PREFILL_FIRST, optional prefill-row and
-    long-prefill caps."""
+    long-prefill caps, offloading, prefix caching."""
 
     def __init__(self, *, block_size: int, num_blocks: int, max_batch_tokens: int,
                  max_requests_per_batch: int, max_blocks_per_seq: int,
                  max_prefill_chunk: int = 0, safety_margin: float = 0.15,
                  free_list: Optional[Sequence[int]] = None, policy: int = POLICY_FIFO,
                  max_prefill_reqs: int = 0, long_prefill_tokens: int = 0,
-                 max_long_prefills: int = 1, offload: bool = False, swap_blocks: int = 0):
+                 max_long_prefills: int = 1, offload: bool = False, swap_blocks: int = 0,
+                 prefix_caching: bool = False):
         self.max_blocks_per_seq = int(max_blocks_per_seq)
         cfg = cb_config(block_size, num_blocks, max_batch_tokens, max_requests_per_batch,
                         max_prefill_chunk, max_blocks_per_seq, float(safety_margin), None,
                         int(policy), int(max_prefill_reqs), int(long_prefill_tokens),
-                        int(max_long_prefills), int(bool(offload)), int(swap_blocks))
+                        int(max_long_prefills), int(bool(offload)), int(swap_blocks),
+                        int(bool(prefix_caching)))
         keep = None
         if free_list is not None:
             keep = np.ascontiguousarray(np.asarray(free_list, dtype=np.int32))
@@ -200,8 +206,25 @@ class Scheduler:
     def __del__(self):
         self.close()
 
-    def add_request(self, req_id: int, prompt_len: int, output_len: int) -> None:
-        _check(_lib.cb_add_request(self._h, req_id, prompt_len, output_len))
+    def add_request(self, req_id: int, prompt_len: int, output_len: int,
+                    tokens: Optional[Sequence[int]] = None) -> None:
+        """``tokens``: ids of the first len(tokens) prompt tokens, for prefix
+        caching (``cb_add_request_tokens``)."""
+        if tokens is None:
+            _check(_lib.cb_add_request(self._h, req_id, prompt_len, output_len))
+            return
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32).reshape(-1))
+        _check(_lib.cb_add_request_tokens(self._h, req_id, prompt_len, output_len,
+                                          t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                          int(t.shape[0])))
+
+    def prefix_stats(self):
+        """(prompt tokens reused so far, keyed blocks, keyed blocks in the
+        initialized pool)."""
+        h, k, p = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(_lib.cb_sched_prefix_stats(self._h, ctypes.byref(h), ctypes.byref(k),
+                                          ctypes.byref(p)))
+        return h.value, k.value, p.value
 
     def add_running_request(self, req_id: int, prompt_len: int, output_len: int,
                             num_cached: int) -> None:

@@ -47,10 +47,31 @@
 // allow, without recomputation), else it is soft-reset: its generated
 // tokens join its prompt, its blocks are freed and it goes to the front of
 // the waiting queue.  A request resumed in a step is not a victim in it.
+//
+// Prefix caching ("Continuous batching architecture", Prefix caching,
+// Eviction), when enabled, for requests queued with their prompt token ids:
+// a block that lies inside the known tokens is keyed, when the step that
+// completes it is committed, by a fingerprint of the whole token prefix up
+// to its end -- so blocks match only as a leading run -- unless another
+// block already holds that key.  A new request reuses the longest leading
+// run of keyed blocks (one prompt token is always left to compute, since
+// the step that completes a prompt yields its first output token), and the
+// reused tokens count as cached.  Blocks are reference-counted.  A freed
+// keyed block keeps its contents and key in an "initialized" pool, still
+// matchable; allocation takes the free queue first and, when it is empty,
+// demotes the newest initialized block (dropping its key).
+//
+// The fingerprint is two 64-bit lanes over the prefix's token ids: FNV-1a
+// (Fowler, Noll, Vo) over their little-endian bytes, and a chain of the
+// splitmix64 output function (Steele, Lea, Flood) over the ids; a match
+// also compares the block's own tokens.  Two different prefixes that end
+// in the same block of tokens would have to agree on all 128 bits to be
+// confused.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <deque>
+#include <list>
 #include <memory>
 #include <new>
 #include <unordered_map>
@@ -65,6 +86,40 @@ std::string& last_error_slot() {
   return s;
 }
 
+struct Fp {
+  uint64_t a = 0, b = 0;
+  bool operator==(const Fp& o) const { return a == o.a && b == o.b; }
+};
+
+struct FpHash {
+  size_t operator()(const Fp& f) const { return (size_t)(f.a ^ (f.b * 0x9E3779B97F4A7C15ull)); }
+};
+
+constexpr uint64_t kFnvOffset = 14695981039346656037ull;
+constexpr uint64_t kFnvPrime = 1099511628211ull;
+
+uint64_t splitmix_out(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Fingerprints of the prefixes ending at each full block of `tokens`.
+std::vector<Fp> prefix_fingerprints(const std::vector<int32_t>& tokens, int32_t bs) {
+  std::vector<Fp> out;
+  Fp h{kFnvOffset, 0};
+  for (size_t i = 0; i < tokens.size(); ++i) {
+    const uint32_t t = (uint32_t)tokens[i];
+    for (int k = 0; k < 4; ++k) {
+      h.a ^= (t >> (8 * k)) & 0xffu;
+      h.a *= kFnvPrime;
+    }
+    h.b = splitmix_out(h.b + 0x9E3779B97F4A7C15ull + t);
+    if ((i + 1) % (size_t)bs == 0) out.push_back(h);
+  }
+  return out;
+}
+
 enum class State { kWaiting, kPrefilling, kDecoding, kFinished, kSwapped };
 
 struct Request {
@@ -77,6 +132,13 @@ struct Request {
   std::vector<int32_t> blocks;
   std::vector<int32_t> swap_slots;    // while swapped: slot of each block
   State resume_state = State::kWaiting;
+  // prefix caching: known prompt token ids, the fingerprint of each full
+  // block of them (prefix up to the block's end), leading blocks already
+  // considered for keys
+  std::vector<int32_t> tokens;
+  bool has_tokens = false;
+  std::vector<Fp> fps;
+  size_t num_registered = 0;
 };
 
 struct Scheduled {
@@ -105,6 +167,15 @@ struct cb_sched {
   std::deque<int32_t> swap_free;
   std::vector<cb::Request*> swapped;  // offload order
   std::vector<int32_t> swap_in_slots, swap_in_blocks, swap_out_blocks, swap_out_slots;
+  // block pool state for prefix caching (reference counts are kept always)
+  std::vector<int32_t> refs;                       // users of each block
+  std::list<int32_t> free_init;                    // initialized pool, freed order
+  std::vector<std::list<int32_t>::iterator> init_pos;
+  std::vector<char> in_init, keyed;
+  std::vector<cb::Fp> block_fp;                    // key of a keyed block
+  std::vector<int32_t> block_tokens;               // its own tokens [num_blocks][bs]
+  std::unordered_map<cb::Fp, int32_t, cb::FpHash> index;
+  int64_t prefix_hits = 0;
 };
 
 namespace {
@@ -114,10 +185,64 @@ int64_t blocks_for(const cb_sched* s, int64_t tokens) {
   return (tokens + bs - 1) / bs;
 }
 
-void take_blocks(cb_sched* s, cb::Request* r, int64_t n) {
-  for (int64_t i = 0; i < n; ++i) {
-    r->blocks.push_back(s->free_list.front());
+int64_t num_free(const cb_sched* s) {
+  return (int64_t)s->free_list.size() + (int64_t)s->free_init.size();
+}
+
+// One block for a new user: the free queue's head, else the newest
+// initialized block, demoted (its key dropped).
+int32_t alloc_block(cb_sched* s) {
+  int32_t b;
+  if (!s->free_list.empty()) {
+    b = s->free_list.front();
     s->free_list.pop_front();
+  } else {
+    b = s->free_init.back();
+    s->free_init.pop_back();
+    s->in_init[b] = 0;
+    s->index.erase(s->block_fp[b]);
+    s->keyed[b] = 0;
+  }
+  s->refs[b] = 1;
+  return b;
+}
+
+void take_blocks(cb_sched* s, cb::Request* r, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) r->blocks.push_back(alloc_block(s));
+}
+
+// Drop r's use of its blocks (logical order): a block with no user left goes
+// to the initialized pool if keyed, else to the tail of the free queue.
+void release_blocks(cb_sched* s, cb::Request* r) {
+  for (int32_t b : r->blocks) {
+    if (--s->refs[b] > 0) continue;
+    if (s->keyed[b]) {
+      s->free_init.push_back(b);
+      s->init_pos[b] = std::prev(s->free_init.end());
+      s->in_init[b] = 1;
+    } else {
+      s->free_list.push_back(b);
+    }
+  }
+  r->blocks.clear();
+  r->num_registered = 0;
+}
+
+// Blocks of the longest leading run of r's prompt that are keyed.
+void match_prefix(const cb_sched* s, const cb::Request* r, std::vector<int32_t>* out) {
+  out->clear();
+  if (!s->cfg.prefix_caching || !r->has_tokens) return;
+  const int64_t bs = s->cfg.block_size;
+  const int64_t limit = std::min<int64_t>((int64_t)r->tokens.size(), (int64_t)r->prompt_len - 1);
+  for (size_t i = 0; (int64_t)(i + 1) * bs <= limit; ++i) {
+    auto it = s->index.find(r->fps[i]);
+    if (it == s->index.end()) break;
+    const int32_t b = it->second;
+    if (!std::equal(r->tokens.begin() + (std::ptrdiff_t)(i * bs),
+                    r->tokens.begin() + (std::ptrdiff_t)((i + 1) * bs),
+                    s->block_tokens.begin() + (std::ptrdiff_t)b * bs))
+      break;
+    out->push_back(b);
   }
 }
 
@@ -202,8 +327,7 @@ void offload_request(cb_sched* s, cb::Request* r) {
     r->state = cb::State::kWaiting;
     s->waiting.push_front(r);
   }
-  for (int32_t b : r->blocks) s->free_list.push_back(b);
-  r->blocks.clear();
+  release_blocks(s, r);
 }
 
 }  // namespace
@@ -236,7 +360,7 @@ void schedule_pass(cb_sched* s, int32_t* num_decodes) {
       if (r->state != cb::State::kDecoding) continue;
       if (budget == 0 || rows() == cap) break;
       const int64_t need = blocks_for(s, (int64_t)r->num_cached + 1) - (int64_t)r->blocks.size();
-      if (need > (int64_t)s->free_list.size()) {
+      if (need > num_free(s)) {
         stall(r, need);
         continue;
       }
@@ -253,7 +377,7 @@ void schedule_pass(cb_sched* s, int32_t* num_decodes) {
       int64_t n = std::min<int64_t>(r->prompt_len - r->num_cached, budget);
       if (chunk_cap > 0) n = std::min(n, chunk_cap);
       const int64_t need = blocks_for(s, r->num_cached + n) - (int64_t)r->blocks.size();
-      if (need > (int64_t)s->free_list.size()) {
+      if (need > num_free(s)) {
         stall(r, need);
         continue;
       }
@@ -264,6 +388,7 @@ void schedule_pass(cb_sched* s, int32_t* num_decodes) {
   };
   // waiting requests, arrival order, head-of-line except long prompts held
   // back by the long-prefill cap
+  std::vector<int32_t> shared;
   auto admissions = [&] {
     size_t i = 0;
     while (i < s->waiting.size() && budget > 0 && rows() < cap && !prefill_cap_hit()) {
@@ -277,11 +402,28 @@ void schedule_pass(cb_sched* s, int32_t* num_decodes) {
           continue;
         }
       }
-      int64_t n = std::min<int64_t>(r->prompt_len, budget);
+      match_prefix(s, r, &shared);
+      const int64_t m = (int64_t)shared.size() * s->cfg.block_size;
+      int64_t n = std::min<int64_t>(r->prompt_len - m, budget);
       if (chunk_cap > 0) n = std::min(n, chunk_cap);
-      const int64_t need = blocks_for(s, n);
-      if ((int64_t)s->free_list.size() - need < s->reserved_blocks) break;
+      const int64_t need = blocks_for(s, m + n) - (int64_t)shared.size();
+      int64_t from_pool = 0;
+      for (int32_t b : shared) from_pool += s->refs[b] == 0;
+      if (num_free(s) - from_pool - need < s->reserved_blocks) break;
       s->waiting.erase(s->waiting.begin() + (std::ptrdiff_t)i);
+      for (int32_t b : shared) {
+        if (s->refs[b] > 0) {
+          ++s->refs[b];
+        } else {
+          s->free_init.erase(s->init_pos[b]);
+          s->in_init[b] = 0;
+          s->refs[b] = 1;
+        }
+      }
+      r->blocks = shared;
+      r->num_cached = (int32_t)m;
+      r->num_registered = shared.size();
+      s->prefix_hits += m;
       take_blocks(s, r, need);
       r->state = cb::State::kPrefilling;
       s->running.push_back(r);
@@ -333,6 +475,14 @@ cb_status cb_sched_create(const cb_config* cfg, cb_sched** out) {
   s->cfg.initial_free_list = nullptr;
   s->reserved_blocks = (int64_t)std::ceil((double)cfg->safety_margin * (double)cfg->num_blocks);
   for (int32_t i = 0; i < cfg->swap_blocks; ++i) s->swap_free.push_back(i);
+  s->refs.assign(cfg->num_blocks, 0);
+  s->init_pos.resize(cfg->num_blocks);
+  s->in_init.assign(cfg->num_blocks, 0);
+  s->keyed.assign(cfg->num_blocks, 0);
+  if (cfg->prefix_caching) {
+    s->block_fp.resize(cfg->num_blocks);
+    s->block_tokens.assign((size_t)cfg->num_blocks * cfg->block_size, 0);
+  }
   if (cfg->initial_free_list) {
     std::vector<char> seen(cfg->num_blocks, 0);
     for (int32_t i = 0; i < cfg->num_blocks; ++i) {
@@ -364,6 +514,22 @@ cb_status cb_add_request(cb_sched* s, int64_t req_id, int32_t prompt_len, int32_
   return CB_OK;
 }
 
+cb_status cb_add_request_tokens(cb_sched* s, int64_t req_id, int32_t prompt_len,
+                                int32_t output_len, const int32_t* tokens, int32_t num_tokens) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  if (num_tokens < 0 || num_tokens > prompt_len || (num_tokens > 0 && !tokens))
+    return cb::fail(CB_ERR_INVALID_ARG, "num_tokens must be in [0, prompt_len] with tokens given");
+  cb_status st = cb_add_request(s, req_id, prompt_len, output_len);
+  if (st != CB_OK) return st;
+  cb::Request* r = s->requests[req_id].get();
+  r->has_tokens = true;
+  if (s->cfg.prefix_caching) {
+    r->tokens.assign(tokens, tokens + num_tokens);
+    r->fps = cb::prefix_fingerprints(r->tokens, s->cfg.block_size);
+  }
+  return CB_OK;
+}
+
 cb_status cb_add_running_request(cb_sched* s, int64_t req_id, int32_t prompt_len,
                                  int32_t output_len, int32_t num_cached) {
   if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
@@ -373,7 +539,7 @@ cb_status cb_add_running_request(cb_sched* s, int64_t req_id, int32_t prompt_len
     return cb::fail(CB_ERR_INVALID_ARG, "num_cached must be in [0, prompt_len + output_len - 2]");
   if (s->step_open) return cb::fail(CB_ERR_STATE, "a step is open; call cb_step_done first");
   const int64_t need = blocks_for(s, num_cached);
-  if (need > (int64_t)s->free_list.size())
+  if (need > num_free(s))
     return cb::fail(CB_ERR_NO_BLOCKS, "not enough free blocks to resume request %lld", (long long)req_id);
   auto r = std::make_unique<cb::Request>();
   r->id = req_id;
@@ -406,11 +572,10 @@ cb_status cb_schedule_step(cb_sched* s, cb_step* out) {
     while (!s->swapped.empty()) {
       cb::Request* r = s->swapped.front();
       const int64_t need = (int64_t)r->swap_slots.size();
-      if ((int64_t)s->free_list.size() - need < s->reserved_blocks) break;
+      if (num_free(s) - need < s->reserved_blocks) break;
       s->swapped.erase(s->swapped.begin());
       for (int32_t slot : r->swap_slots) {
-        const int32_t b = s->free_list.front();
-        s->free_list.pop_front();
+        const int32_t b = alloc_block(s);
         r->blocks.push_back(b);
         s->swap_in_slots.push_back(slot);
         s->swap_in_blocks.push_back(b);
@@ -458,7 +623,7 @@ cb_status cb_schedule_step(cb_sched* s, cb_step* out) {
     for (cb::Request* r : order) {
       int64_t total = 0;
       for (const auto& d : demand) total += d.second;
-      if ((int64_t)s->free_list.size() >= total || s->running.size() <= 1) break;
+      if (num_free(s) >= total || s->running.size() <= 1) break;
       for (size_t i = 0; i < demand.size(); ++i)
         if (demand[i].first == r->id) {
           demand.erase(demand.begin() + (std::ptrdiff_t)i);
@@ -499,10 +664,28 @@ cb_status cb_step_done(cb_sched* s, int32_t* num_finished, const int64_t** finis
       done.push_back(r);
     }
   }
+  if (s->cfg.prefix_caching) {
+    // key every block this step completed inside the known tokens
+    const size_t bs = (size_t)s->cfg.block_size;
+    for (const cb::Scheduled& e : s->batch) {
+      cb::Request* r = e.req;
+      if (!r->has_tokens) continue;
+      const size_t full = std::min<size_t>((size_t)r->num_cached, r->tokens.size()) / bs;
+      for (; r->num_registered < full; ++r->num_registered) {
+        const size_t i = r->num_registered;
+        const int32_t b = r->blocks[i];
+        if (!s->index.emplace(r->fps[i], b).second) continue;
+        s->keyed[b] = 1;
+        s->block_fp[b] = r->fps[i];
+        std::copy(r->tokens.begin() + (std::ptrdiff_t)(i * bs),
+                  r->tokens.begin() + (std::ptrdiff_t)((i + 1) * bs),
+                  s->block_tokens.begin() + (std::ptrdiff_t)b * (std::ptrdiff_t)bs);
+      }
+    }
+  }
   for (cb::Request* r : done) {
     s->running.erase(std::find(s->running.begin(), s->running.end(), r));
-    for (int32_t b : r->blocks) s->free_list.push_back(b);
-    r->blocks.clear();
+    release_blocks(s, r);
     s->finished_ids.push_back(r->id);
     s->requests.erase(r->id);
   }
@@ -532,7 +715,7 @@ cb_status cb_request_slots(const cb_sched* s, int64_t req_id, int32_t start, int
 cb_status cb_sched_counts(const cb_sched* s, int32_t* free_blocks, int32_t* num_waiting,
                           int32_t* num_running) {
   if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
-  if (free_blocks) *free_blocks = (int32_t)s->free_list.size();
+  if (free_blocks) *free_blocks = (int32_t)num_free(s);
   if (num_waiting) *num_waiting = (int32_t)s->waiting.size();
   if (num_running) *num_running = (int32_t)s->running.size();
   return CB_OK;
@@ -551,12 +734,28 @@ cb_status cb_sched_swapped(const cb_sched* s, int64_t* out, int32_t capacity, in
 
 cb_status cb_sched_free_list(const cb_sched* s, int32_t* out, int32_t capacity, int32_t* count) {
   if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
-  const int32_t n = (int32_t)s->free_list.size();
+  const int32_t n = (int32_t)num_free(s);
   if (count) *count = n;
   if (out) {
-    const int32_t m = std::min(n, capacity);
-    for (int32_t i = 0; i < m; ++i) out[i] = s->free_list[i];
+    int32_t i = 0;
+    for (int32_t b : s->free_list) {
+      if (i >= capacity) break;
+      out[i++] = b;
+    }
+    for (int32_t b : s->free_init) {
+      if (i >= capacity) break;
+      out[i++] = b;
+    }
   }
+  return CB_OK;
+}
+
+cb_status cb_sched_prefix_stats(const cb_sched* s, int64_t* hit_tokens, int32_t* keyed_blocks,
+                                int32_t* pool_blocks) {
+  if (!s) return cb::fail(CB_ERR_INVALID_ARG, "scheduler is NULL");
+  if (hit_tokens) *hit_tokens = s->prefix_hits;
+  if (keyed_blocks) *keyed_blocks = (int32_t)s->index.size();
+  if (pool_blocks) *pool_blocks = (int32_t)s->free_init.size();
   return CB_OK;
 }
 

@@ -19,8 +19,8 @@ import torch
 import workloads
 from oracle import attention as oatt
 from oracle import paged_kv
-from tests.sched_driver import (c_from_config, load_scenario, normalize, oracle_from_config,
-                                scenario_to_config)
+from tests.sched_driver import (add_waiting, c_from_config, load_scenario, normalize,
+                                oracle_from_config, scenario_to_config)
 
 TOL = {"f32": (1e-4, 0.0), "bf16": (2e-2, 1e-2)}
 
@@ -129,8 +129,8 @@ class ParityRun:
             while (self.next_arrival < len(sc.waiting) and
                    sc.waiting[self.next_arrival].arrival_step <= self.step_idx):
                 w = sc.waiting[self.next_arrival]
-                self.o.add_request(w.req_id, w.prompt_len, w.output_len)
-                self.c.add_request(w.req_id, w.prompt_len, w.output_len)
+                add_waiting(self.o, w)
+                add_waiting(self.c, w)
                 self.next_arrival += 1
         so = self.o.schedule_step()
         sg = self.c.schedule_step()

@@ -35,7 +35,8 @@ def oracle_from_config(cfg: dict):
                          max_prefill_reqs=cfg.get("max_prefill_reqs", 0),
                          long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
                          max_long_prefills=cfg.get("max_long_prefills", 1),
-                         offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0))
+                         offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0),
+                         prefix_caching=cfg.get("prefix_caching", False))
 
 
 def run_trace(sched, requests, num_steps, arrivals=None):
@@ -48,7 +49,10 @@ def run_trace(sched, requests, num_steps, arrivals=None):
     for s in range(num_steps):
         while i < len(pending) and pending[i].get("arrival_step", 0) <= s:
             r = pending[i]
-            sched.add_request(r["id"], r["prompt_len"], r["output_len"])
+            if r.get("tokens") is not None:
+                sched.add_request(r["id"], r["prompt_len"], r["output_len"], tokens=r["tokens"])
+            else:
+                sched.add_request(r["id"], r["prompt_len"], r["output_len"])
             i += 1
         st = normalize(sched.schedule_step())
         if st["status"] == 0:
@@ -67,7 +71,8 @@ def scenario_to_config(sc) -> dict:
             "safety_margin": sc.safety_margin,
             "max_blocks_per_seq": sc.max_blocks_per_seq,
             "free_list": [int(x) for x in sc.free_list],
-            "policy": sc.policy, "offload": sc.offload, "swap_blocks": sc.swap_blocks}
+            "policy": sc.policy, "offload": sc.offload, "swap_blocks": sc.swap_blocks,
+            "prefix_caching": sc.prefix_caching}
 
 
 def c_from_config(cfg: dict):
@@ -81,7 +86,8 @@ def c_from_config(cfg: dict):
                         policy=cfg.get("policy", 0), max_prefill_reqs=cfg.get("max_prefill_reqs", 0),
                         long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
                         max_long_prefills=cfg.get("max_long_prefills", 1),
-                        offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0))
+                        offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0),
+                        prefix_caching=cfg.get("prefix_caching", False))
 
 
 def load_scenario(sched, sc, up_to_step=None):
@@ -91,4 +97,12 @@ def load_scenario(sched, sc, up_to_step=None):
         sched.add_running_request(r.req_id, r.prompt_len, r.output_len, r.num_cached)
     for w in sc.waiting:
         if up_to_step is None or w.arrival_step <= up_to_step:
-            sched.add_request(w.req_id, w.prompt_len, w.output_len)
+            add_waiting(sched, w)
+
+
+def add_waiting(sched, w):
+    """Queue a workloads.WaitingRequest (with its token ids, if any)."""
+    if w.tokens is not None:
+        sched.add_request(w.req_id, w.prompt_len, w.output_len, tokens=w.tokens)
+    else:
+        sched.add_request(w.req_id, w.prompt_len, w.output_len)

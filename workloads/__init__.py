@@ -56,6 +56,7 @@ class WaitingRequest:
     prompt_len: int
     output_len: int
     arrival_step: int = 0    # step at which the request joins the queue
+    tokens: Optional[np.ndarray] = None  # synthetic prompt token ids (prefix caching)
 
 
 @dataclasses.dataclass
@@ -81,6 +82,7 @@ class Scenario:
     policy: int = 0                  # 0 FIFO, 1 PrefillFirst
     offload: bool = False            # offload requests when blocks run out
     swap_blocks: int = 0             # CPU swap pool capacity in blocks
+    prefix_caching: bool = False     # share blocks of equal prompt prefixes
 
     def __post_init__(self):
         longest = max([r.prompt_len + r.output_len - 1 for r in self.running]
@@ -243,6 +245,35 @@ def offload_pressure(seed: int = 0, num_requests: int = 24, num_blocks: int = 40
         offload=True, swap_blocks=swap_blocks)
 
 
+def shared_prefix(seed: int = 0, num_requests: int = 48, num_system: int = 4,
+                  num_blocks: int = 4096, num_layers: int = 2) -> Scenario:
+    """Requests that share long prompt prefixes (a few "system prompts"),
+    for prefix caching: 4 system prompts of U[200, 1200] synthetic token ids
+    (vocabulary 32,000), each request one of them plus its own U[16, 400]
+    suffix, outputs U[8, 64]; arrivals over the first 16 steps; 32 Q / 8 KV
+    heads, D = 128, bf16, budget 2048 tokens."""
+    rng = np.random.default_rng(seed)
+    systems = [rng.integers(0, 32000, size=int(rng.integers(200, 1200, endpoint=True)))
+               for _ in range(num_system)]
+    waiting = []
+    for i in range(num_requests):
+        sysp = systems[int(rng.integers(0, num_system))]
+        toks = np.concatenate([sysp, rng.integers(0, 32000, size=int(rng.integers(16, 400,
+                                                                                 endpoint=True)))])
+        waiting.append(WaitingRequest(req_id=i, prompt_len=int(len(toks)),
+                                      output_len=int(rng.integers(8, 64, endpoint=True)),
+                                      arrival_step=int(rng.integers(0, 16)),
+                                      tokens=toks.astype(np.int32)))
+    waiting.sort(key=lambda w: w.arrival_step)
+    return Scenario(
+        name="shared_prefix", num_q_heads=32, num_kv_heads=8, head_dim=128,
+        dtype="bf16", num_blocks=num_blocks, max_batch_tokens=2048,
+        max_requests_per_batch=64, max_prefill_chunk=0, safety_margin=0.0,
+        max_blocks_per_seq=0, free_list=permuted_free_list(num_blocks, seed + 1),
+        running=[], waiting=waiting, num_layers=num_layers, value_scale=1.0, seed=seed,
+        prefix_caching=True)
+
+
 SCENARIOS = {
     "chunked_prefill_1000": chunked_prefill_1000,
     "decode_64": decode_64,
@@ -251,6 +282,7 @@ SCENARIOS = {
     "trace_2000": trace_2000,
     "prefill_chunk_16k": prefill_chunk_16k,
     "offload_pressure": offload_pressure,
+    "shared_prefix": shared_prefix,
 }
 
 

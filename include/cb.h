@@ -166,6 +166,20 @@ typedef struct cb_config {
                                      queue first and then demotes the NEWEST
                                      initialized block (its key dropped).
                                      Free capacity counts both. */
+  int32_t sliding_window;         /* W > 0: every layer served by this pool
+                                     is a sliding-window layer ("Continuous
+                                     batching architecture", Memory
+                                     management): a query at position p
+                                     reads keys p-W+1..p only.  After each
+                                     committed step, pages of a running
+                                     request that lie wholly before
+                                     num_cached - W + 1 are recycled (to the
+                                     free queue's tail, batch order then
+                                     table order, before finished requests
+                                     release theirs) and their table entries
+                                     become -1.  Only live pages are swapped.
+                                     Not combinable with prefix_caching.
+                                     0 = full attention. */
 } cb_config;
 
 #define CB_POLICY_FIFO 0

@@ -42,6 +42,9 @@ Follows:
   freed blocks keep their content and key ("initialized") so later requests
   can still match them, and when uninitialized blocks run out the newest
   initialized ones are demoted (key dropped) and reused.
+* *Continuous batching architecture*, Memory management (sliding
+  attention): sliding-window layers keep only a fixed window of recent
+  tokens by recycling a small set of pages, and do not share blocks.
 * vLLM performance-series post (page 5), "Request-parallel prefill": several
   requests may prefill in one batch, but only a limited number of LONG
   prompts at a time, so short prompts are not held behind a long one.
@@ -110,6 +113,20 @@ Readings where the pages leave a step open:
    requests release their blocks the same way; blocks swapped back in are
    new private blocks.
 
+13. Sliding window (``sliding_window`` = W > 0; the whole pool serves
+   sliding layers -- a model mixing full and sliding layers would need a
+   second pool): a query at position p reads keys p-W+1 .. p, so once a
+   request has num_cached tokens, its pages whose last position is below
+   num_cached - W + 1 are never read again.  At step_done, after the state
+   updates, such pages of every request of the batch that did not finish
+   are freed (batch order, then logical order) to the free queue's tail and
+   their table entries become -1; then finished requests release their
+   remaining pages.  Block demand still counts table entries (dropped ones
+   included), so a request holds at most ceil((W - 1) / bs) + 1 pages
+   plus its next chunk.  Only live pages are swapped out (and back in, to new
+   blocks at the same table positions).  Prefix caching is refused with a
+   window (sliding layers do not share blocks).
+
 Parity: pinned by hand-derived traces (tests/golden/scheduler_*.json) and by
 invariants (budget, cap, FIFO order, block conservation, all-or-nothing
 admission); the full batch composition beyond the pages' rules rests on the
@@ -141,6 +158,7 @@ class Request:
         self.blocks: List[int] = []
         self.state = WAITING
         self.swap_slots: List[int] = []
+        self.swapped_table: List[bool] = []   # while swapped: live entries
         self.resume_state = None
         self.tokens = None        # known prompt token ids (prefix caching)
         self.num_registered = 0   # leading blocks already considered for keys
@@ -155,7 +173,7 @@ class FifoScheduler:
                  policy: int = POLICY_FIFO, max_prefill_reqs: int = 0,
                  long_prefill_tokens: int = 0, max_long_prefills: int = 1,
                  offload: bool = False, swap_blocks: int = 0,
-                 prefix_caching: bool = False):
+                 prefix_caching: bool = False, sliding_window: int = 0):
         self.block_size = int(block_size)
         self.num_blocks = int(num_blocks)
         self.max_batch_tokens = int(max_batch_tokens)
@@ -177,6 +195,11 @@ class FifoScheduler:
         # prefix caching: reference counts of blocks in use, keyed blocks
         # (key = token prefix up to the block's end) and the initialized pool
         self.prefix_caching = bool(prefix_caching)
+        self.sliding_window = int(sliding_window)
+        if self.sliding_window < 0:
+            raise ValueError("sliding_window must be >= 0")
+        if self.sliding_window and self.prefix_caching:
+            raise ValueError("sliding-window layers do not share blocks")
         self.refs: Dict[int, int] = {}
         self.cache_index: Dict[tuple, int] = {}
         self.block_key: Dict[int, tuple] = {}
@@ -222,6 +245,8 @@ class FifoScheduler:
 
     def _release(self, r) -> None:
         for b in r.blocks:
+            if b < 0:
+                continue                      # dropped out of the window
             self.refs[b] -= 1
             if self.refs[b] == 0:
                 del self.refs[b]
@@ -391,9 +416,11 @@ class FifoScheduler:
         """Take an active request off the GPU: to the swap pool if it has room
         for all its blocks, else a soft reset."""
         self.running.remove(r)
-        if self.swap_free and len(self.swap_free) >= len(r.blocks):
-            r.swap_slots = [self.swap_free.popleft() for _ in r.blocks]
-            swap_out.extend(zip(r.blocks, r.swap_slots))
+        live = [b for b in r.blocks if b >= 0]
+        if self.swap_free and len(self.swap_free) >= len(live):
+            r.swap_slots = [self.swap_free.popleft() for _ in live]
+            swap_out.extend(zip(live, r.swap_slots))
+            r.swapped_table = [b >= 0 for b in r.blocks]
             r.resume_state = r.state
             r.state = SWAPPED
             self.swapped.append(r)
@@ -419,7 +446,12 @@ class FifoScheduler:
                 if self._num_free() - need < self.reserved_blocks:
                     break
                 del self.swapped[0]
-                for slot in r.swap_slots:
+                slots = iter(r.swap_slots)
+                for was_live in r.swapped_table:
+                    if not was_live:
+                        r.blocks.append(-1)
+                        continue
+                    slot = next(slots)
                     b = self._alloc()
                     r.blocks.append(b)
                     swap_in.append((slot, b))
@@ -520,6 +552,21 @@ class FifoScheduler:
                         self.cache_index[key] = r.blocks[i]
                         self.block_key[r.blocks[i]] = key
                     r.num_registered += 1
+        if self.sliding_window > 0:
+            # pages wholly before every future query's window go back
+            bs = self.block_size
+            for r, _ in self._pending:
+                if r.state == FINISHED:
+                    continue
+                lo = max(0, r.num_cached - self.sliding_window + 1) // bs
+                for j in range(min(lo, len(r.blocks))):
+                    b = r.blocks[j]
+                    if b >= 0:
+                        self.refs[b] -= 1
+                        if self.refs[b] == 0:
+                            del self.refs[b]
+                            self.free.append(b)
+                        r.blocks[j] = -1
         for r in finished:
             self.running.remove(r)
             self._release(r)

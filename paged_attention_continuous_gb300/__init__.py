@@ -63,7 +63,7 @@ class cb_config(ctypes.Structure):
                 ("policy", ctypes.c_int32), ("max_prefill_reqs", ctypes.c_int32),
                 ("long_prefill_tokens", ctypes.c_int32), ("max_long_prefills", ctypes.c_int32),
                 ("offload", ctypes.c_int32), ("swap_blocks", ctypes.c_int32),
-                ("prefix_caching", ctypes.c_int32)]
+                ("prefix_caching", ctypes.c_int32), ("sliding_window", ctypes.c_int32)]
 
 
 class cb_step(ctypes.Structure):
@@ -173,7 +173,8 @@ POLICY_FIFO, POLICY_PREFILL_FIRST = 0, 1
 class Scheduler:
     """Continuous-batching scheduler (C++), see ``cb_schedule_step``:
     policy FIFO (default) or PREFILL_FIRST, optional prefill-row and
-    long-prefill caps, offloading, prefix caching."""
+    long-prefill caps, offloading, prefix caching, sliding-window page
+    recycling."""
 
     def __init__(self, *, block_size: int, num_blocks: int, max_batch_tokens: int,
                  max_requests_per_batch: int, max_blocks_per_seq: int,
@@ -181,13 +182,13 @@ class Scheduler:
                  free_list: Optional[Sequence[int]] = None, policy: int = POLICY_FIFO,
                  max_prefill_reqs: int = 0, long_prefill_tokens: int = 0,
                  max_long_prefills: int = 1, offload: bool = False, swap_blocks: int = 0,
-                 prefix_caching: bool = False):
+                 prefix_caching: bool = False, sliding_window: int = 0):
         self.max_blocks_per_seq = int(max_blocks_per_seq)
         cfg = cb_config(block_size, num_blocks, max_batch_tokens, max_requests_per_batch,
                         max_prefill_chunk, max_blocks_per_seq, float(safety_margin), None,
                         int(policy), int(max_prefill_reqs), int(long_prefill_tokens),
                         int(max_long_prefills), int(bool(offload)), int(swap_blocks),
-                        int(bool(prefix_caching)))
+                        int(bool(prefix_caching)), int(sliding_window))
         keep = None
         if free_list is not None:
             keep = np.ascontiguousarray(np.asarray(free_list, dtype=np.int32))

@@ -61,6 +61,13 @@
 // matchable; allocation takes the free queue first and, when it is empty,
 // demotes the newest initialized block (dropping its key).
 //
+// Sliding-window layers ("Continuous batching architecture", Memory
+// management: they keep a fixed window of recent tokens by recycling a small
+// set of pages), when the pool serves such layers: a query at position p
+// reads keys p-W+1..p, so after each committed step the pages of a running
+// request that lie wholly before num_cached - W + 1 go back to the free
+// queue and their table entries become -1.
+//
 // The fingerprint is two 64-bit lanes over the prefix's token ids: FNV-1a
 // (Fowler, Noll, Vo) over their little-endian bytes, and a chain of the
 // splitmix64 output function (Steele, Lea, Flood) over the ids; a match
@@ -130,7 +137,8 @@ struct Request {
   int32_t num_generated = 0;  // output tokens produced so far
   State state = State::kWaiting;
   std::vector<int32_t> blocks;
-  std::vector<int32_t> swap_slots;    // while swapped: slot of each block
+  std::vector<int32_t> swap_slots;    // while swapped: slot of each live block
+  std::vector<char> swapped_live;     // while swapped: table entry was live
   State resume_state = State::kWaiting;
   // prefix caching: known prompt token ids, the fingerprint of each full
   // block of them (prefix up to the block's end), leading blocks already
@@ -215,6 +223,7 @@ void take_blocks(cb_sched* s, cb::Request* r, int64_t n) {
 // to the initialized pool if keyed, else to the tail of the free queue.
 void release_blocks(cb_sched* s, cb::Request* r) {
   for (int32_t b : r->blocks) {
+    if (b < 0) continue;  // recycled out of the window
     if (--s->refs[b] > 0) continue;
     if (s->keyed[b]) {
       s->free_init.push_back(b);
@@ -307,9 +316,14 @@ void emit_step(cb_sched* s, int32_t num_decodes, cb_step* out) {
 // hold all its blocks, else a soft reset.
 void offload_request(cb_sched* s, cb::Request* r) {
   s->running.erase(std::find(s->running.begin(), s->running.end(), r));
-  if (!s->swap_free.empty() && s->swap_free.size() >= r->blocks.size()) {
+  size_t live = 0;
+  for (int32_t b : r->blocks) live += b >= 0;
+  if (!s->swap_free.empty() && s->swap_free.size() >= live) {
     r->swap_slots.clear();
+    r->swapped_live.clear();
+    for (int32_t b : r->blocks) r->swapped_live.push_back(b >= 0);
     for (int32_t b : r->blocks) {
+      if (b < 0) continue;
       const int32_t slot = s->swap_free.front();
       s->swap_free.pop_front();
       r->swap_slots.push_back(slot);
@@ -463,8 +477,10 @@ cb_status cb_sched_create(const cb_config* cfg, cb_sched** out) {
   if (cfg->block_size <= 0 || cfg->num_blocks <= 0 || cfg->max_batch_tokens <= 0 ||
       cfg->max_requests_per_batch <= 0 || cfg->max_blocks_per_seq <= 0 ||
       cfg->max_prefill_chunk < 0 || cfg->max_prefill_reqs < 0 || cfg->long_prefill_tokens < 0 ||
-      cfg->max_long_prefills < 0 || cfg->swap_blocks < 0)
+      cfg->max_long_prefills < 0 || cfg->swap_blocks < 0 || cfg->sliding_window < 0)
     return cb::fail(CB_ERR_INVALID_ARG, "config sizes must be positive");
+  if (cfg->sliding_window > 0 && cfg->prefix_caching)
+    return cb::fail(CB_ERR_INVALID_ARG, "sliding-window layers do not share blocks (prefix_caching)");
   if (cfg->policy != CB_POLICY_FIFO && cfg->policy != CB_POLICY_PREFILL_FIRST)
     return cb::fail(CB_ERR_INVALID_ARG, "unknown policy %d", cfg->policy);
   if (!(cfg->safety_margin >= 0.0f) || cfg->safety_margin > 1.0f)
@@ -574,7 +590,13 @@ cb_status cb_schedule_step(cb_sched* s, cb_step* out) {
       const int64_t need = (int64_t)r->swap_slots.size();
       if (num_free(s) - need < s->reserved_blocks) break;
       s->swapped.erase(s->swapped.begin());
-      for (int32_t slot : r->swap_slots) {
+      size_t k = 0;
+      for (char was_live : r->swapped_live) {
+        if (!was_live) {
+          r->blocks.push_back(-1);
+          continue;
+        }
+        const int32_t slot = r->swap_slots[k++];
         const int32_t b = alloc_block(s);
         r->blocks.push_back(b);
         s->swap_in_slots.push_back(slot);
@@ -680,6 +702,23 @@ cb_status cb_step_done(cb_sched* s, int32_t* num_finished, const int64_t** finis
         std::copy(r->tokens.begin() + (std::ptrdiff_t)(i * bs),
                   r->tokens.begin() + (std::ptrdiff_t)((i + 1) * bs),
                   s->block_tokens.begin() + (std::ptrdiff_t)b * (std::ptrdiff_t)bs);
+      }
+    }
+  }
+  if (s->cfg.sliding_window > 0) {
+    // pages wholly before every future query's window go back
+    const int64_t bs = s->cfg.block_size;
+    for (const cb::Scheduled& e : s->batch) {
+      cb::Request* r = e.req;
+      if (r->state == cb::State::kFinished) continue;
+      const int64_t lo =
+          std::min<int64_t>(std::max<int64_t>(0, (int64_t)r->num_cached - s->cfg.sliding_window + 1) / bs,
+                            (int64_t)r->blocks.size());
+      for (int64_t j = 0; j < lo; ++j) {
+        const int32_t b = r->blocks[j];
+        if (b < 0) continue;
+        if (--s->refs[b] == 0) s->free_list.push_back(b);
+        r->blocks[j] = -1;
       }
     }
   }

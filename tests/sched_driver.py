@@ -36,7 +36,8 @@ def oracle_from_config(cfg: dict):
                          long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
                          max_long_prefills=cfg.get("max_long_prefills", 1),
                          offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0),
-                         prefix_caching=cfg.get("prefix_caching", False))
+                         prefix_caching=cfg.get("prefix_caching", False),
+                         sliding_window=cfg.get("sliding_window", 0))
 
 
 def run_trace(sched, requests, num_steps, arrivals=None):
@@ -72,7 +73,7 @@ def scenario_to_config(sc) -> dict:
             "max_blocks_per_seq": sc.max_blocks_per_seq,
             "free_list": [int(x) for x in sc.free_list],
             "policy": sc.policy, "offload": sc.offload, "swap_blocks": sc.swap_blocks,
-            "prefix_caching": sc.prefix_caching}
+            "prefix_caching": sc.prefix_caching, "sliding_window": sc.sliding_window}
 
 
 def c_from_config(cfg: dict):
@@ -87,7 +88,8 @@ def c_from_config(cfg: dict):
                         long_prefill_tokens=cfg.get("long_prefill_tokens", 0),
                         max_long_prefills=cfg.get("max_long_prefills", 1),
                         offload=cfg.get("offload", False), swap_blocks=cfg.get("swap_blocks", 0),
-                        prefix_caching=cfg.get("prefix_caching", False))
+                        prefix_caching=cfg.get("prefix_caching", False),
+                        sliding_window=cfg.get("sliding_window", 0))
 
 
 def load_scenario(sched, sc, up_to_step=None):

@@ -83,6 +83,7 @@ class Scenario:
     offload: bool = False            # offload requests when blocks run out
     swap_blocks: int = 0             # CPU swap pool capacity in blocks
     prefix_caching: bool = False     # share blocks of equal prompt prefixes
+    sliding_window: int = 0          # > 0: every layer attends the last W tokens
 
     def __post_init__(self):
         longest = max([r.prompt_len + r.output_len - 1 for r in self.running]

@@ -352,6 +352,7 @@ cb_status cb_kv_swap(const cb_swap_args* args, cb_stream_t stream);
  * Rows [0, num_decodes) must have query length 1 and run the split-KV decode
  * kernel (which also merges the splits of requests whose cache it split);
  * the remaining rows run the prefill-chunk kernel.  Both go to `stream`.
+ * With sliding_window = W > 0 the sum runs over j = p-W+1..p instead.
  * A row with query length 0 and seq_len 0 is padding and is skipped (no
  * error bit), so a step may be padded to a fixed shape (row counts, token
  * count, max_q_len) and captured once in a CUDA graph; padded tokens carry
@@ -383,6 +384,12 @@ typedef struct cb_attention_args {
                                    cb_attention_workspace_init; calls leave it
                                    ready for the next call */
   size_t workspace_bytes;
+  int32_t sliding_window;       /* W > 0: sliding-window layer ("Continuous
+                                   batching architecture", Memory management)
+                                   -- query position p attends keys
+                                   p-W+1..p only, and table entries of pages
+                                   wholly before a row's window are never
+                                   read (they may be -1); 0: full attention */
 } cb_attention_args;
 
 /* Device error bits (cb_attention_read_errors / cb_kv_append error_word). */

@@ -98,6 +98,7 @@ cb_status launch_decode(const cb_attention_args& a, const WsLayout& L, cudaStrea
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.window = a.sliding_window;
   p.error_word = reinterpret_cast<uint32_t*>(ws + L.header);
   p.work_counter = reinterpret_cast<uint32_t*>(ws + L.header) + 1;
   p.merge_counter = reinterpret_cast<uint32_t*>(ws + L.header) + 3;
@@ -150,6 +151,7 @@ cb_status launch_simt_rows(const cb_attention_args& a, const WsLayout& L, int ro
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.window = a.sliding_window;
   p.error_word = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) + L.header);
   const int64_t warps = (int64_t)(tok_end - tok_begin) * a.num_q_heads;
   const int64_t blocks = (warps + 7) / 8;
@@ -220,6 +222,7 @@ extern "C" cb_status cb_paged_attention(const cb_attention_args* args, cb_stream
   if (a.head_dim != 64 && a.head_dim != 128) return fail(CB_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (a.dtype != CB_DTYPE_F32 && a.dtype != CB_DTYPE_BF16) return fail(CB_ERR_INVALID_ARG, "unknown dtype");
   if (a.num_blocks <= 0 || a.max_blocks_per_seq <= 0) return fail(CB_ERR_INVALID_ARG, "bad pool sizes");
+  if (a.sliding_window < 0) return fail(CB_ERR_INVALID_ARG, "sliding_window must be >= 0");
   if (a.max_q_len < 1 || a.max_seq_len < a.max_q_len ||
       (a.max_seq_len + a.block_size - 1) / a.block_size > a.max_blocks_per_seq)
     return fail(CB_ERR_INVALID_ARG, "max_q_len / max_seq_len inconsistent with the block table");

@@ -37,6 +37,13 @@
 //     one per (request, query head), from a second counter: wait (bounded)
 //     until the request's splits are all done -- they are all held by
 //     running warps by then -- and merge them with the log-sum-exp rescale.
+//
+// Sliding-window layers ("Continuous batching architecture", Memory
+// management): with window W > 0 the decode token at position seq_len - 1
+// attends keys seq_len - W .. seq_len - 1 only.  A row's items then cover
+// the pages from the one holding key seq_len - W (pages before it may have
+// been recycled and are never read), and keys before the window on that
+// first page are masked like the slots past the end on the last page.
 #pragma once
 
 #include <cstdint>
@@ -84,6 +91,7 @@ struct Params {
   int32_t num_q_heads;
   int32_t num_kv_heads;
   float scale_log2;        // softmax scale * log2(e)
+  int32_t window;          // sliding window (0: full attention)
   uint32_t* error_word;
   uint32_t* work_counter;  // zero between launches (the last grab resets it)
   uint32_t* merge_counter; // zero between launches (the last grab resets it)
@@ -102,6 +110,10 @@ struct Params {
 struct RowSplit {
   int na, bp, nb;
 };
+
+// First key and first page a decode row of length L reads (window W, 0 = all).
+__device__ __forceinline__ int first_key(int L, int W) { return W > 0 && L > W ? L - W : 0; }
+__device__ __forceinline__ int first_page(int L, int W) { return first_key(L, W) / kPageTokens; }
 
 __device__ __forceinline__ RowSplit row_split(int pages, int spa, int spb) {
   RowSplit s;
@@ -232,7 +244,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
         if (blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_DECODE_QLEN);
       }
     }
-    pages = (L + kPageTokens - 1) / kPageTokens;
+    pages = (L + kPageTokens - 1) / kPageTokens - first_page(L, p.window);
     row_len[i] = L;
     row_tok[i] = q0;
     my_pages += pages;
@@ -264,7 +276,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
     const int e = min(b + seg, p.num_rows);
     int sum_a = 0, sum_b = 0;
     for (int i = b; i < e; ++i) {
-      const RowSplit rs = row_split((row_len[i] + kPageTokens - 1) / kPageTokens, spa0, spb0);
+      const int Li = row_len[i];
+      const RowSplit rs =
+          row_split((Li + kPageTokens - 1) / kPageTokens - first_page(Li, p.window), spa0, spb0);
       const int na = rs.na, nb = rs.nb;
       plan_a[i + 1] = na;
       plan_b[i + 1] = nb;
@@ -402,15 +416,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
       const int r = p.row_begin + i;
       const int L = row_len[i];
       const int pages = (L + kPageTokens - 1) / kPageTokens;
+      const int fp = first_page(L, p.window);
       const int na = a1 - a0;
-      const int bp = na * spa0;
+      const int bp = fp + na * spa0;
       nx_ok = true;
       nx_i = i;
       nx_g = g;
       nx_split = split;
       nx_nsplit = na + (b1 - b0);
       if (phase_a) {
-        nx_page0 = split * spa0;
+        nx_page0 = fp + split * spa0;
         nx_page1 = nx_page0 + spa0;
       } else {
         nx_page0 = bp + split * spb0;
@@ -561,7 +576,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
         m_own = -INFINITY;
         l_own = 0.f;
       }
+      // keys [lo_t, valid) of this page are read: the sequence end on the
+      // last page, the window start on the first
       const int valid = min(kPageTokens, d.seq_len - page * kPageTokens);
+      const int lo_t = first_key(d.seq_len, p.window) - page * kPageTokens;
       const uint8_t* kp = ws.kv[st][0];
       const uint8_t* vp = ws.kv[st][1];
 
@@ -608,7 +626,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
           }
         }
-        sc[it] = (t < valid) ? v[0] : -INFINITY;
+        sc[it] = (t < valid && t >= lo_t) ? v[0] : -INFINITY;
       }
 
       // ---- online softmax (base 2) -------------------------------------------
@@ -639,8 +657,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
 
       // ---- P.V ------------------------------------------------------------------
       // Slots past the sequence end hold whatever the pool held (possibly
-      // not finite), so on a partial page their V rows are zeroed before use;
-      // full pages skip the masking.
+      // not finite), so on a partial page their V rows (and those before the
+      // window) are zeroed before use; full pages skip the masking.
       auto pv = [&](auto mask_tag) {
         constexpr bool kMask = decltype(mask_tag)::value;
 #pragma unroll
@@ -650,7 +668,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
           float ph[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) ph[h] = __shfl_sync(0xffffffffu, pr[it], tok * C::kLG + h * C::kDup);
-          const bool tv = t < valid;
+          const bool tv = t < valid && t >= lo_t;
 #pragma unroll
           for (int c = 0; c < C::kCPL; ++c) {
             float vf[C::kEPC];
@@ -671,7 +689,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
           }
         }
       };
-      if (valid == kPageTokens)
+      if (valid == kPageTokens && lo_t <= 0)
         pv(std::false_type{});
       else
         pv(std::true_type{});

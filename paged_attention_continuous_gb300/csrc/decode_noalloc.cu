@@ -107,6 +107,7 @@ cb_status launch(const cb_attention_args& a, uint8_t* scratch, const NoAllocLayo
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.window = a.sliding_window;
   p.error_word = error_word;
   p.work_counter = reinterpret_cast<uint32_t*>(scratch) + 1;
   p.merge_counter = reinterpret_cast<uint32_t*>(scratch) + 3;
@@ -154,6 +155,7 @@ extern "C" cb_status cb_paged_decode_noalloc(const cb_attention_args* args, uint
   if (a.block_size != 16) return fail(CB_ERR_UNSUPPORTED, "block_size must be 16");
   if (a.dtype != CB_DTYPE_F32 && a.dtype != CB_DTYPE_BF16) return fail(CB_ERR_INVALID_ARG, "unknown dtype");
   if (a.num_blocks <= 0 || a.max_blocks_per_seq <= 0) return fail(CB_ERR_INVALID_ARG, "bad pool sizes");
+  if (a.sliding_window < 0) return fail(CB_ERR_INVALID_ARG, "sliding_window must be >= 0");
   const uintptr_t al = (uintptr_t)a.q | (uintptr_t)a.out | (uintptr_t)a.k_cache | (uintptr_t)a.v_cache;
   if (al & 15u) return fail(CB_ERR_INVALID_ARG, "q/out/cache pointers must be 16-byte aligned");
   if (a.num_reqs > cb::decode::kPlanMax)

@@ -43,6 +43,15 @@
 //              as soon as its own inputs are ready -- each softmax warpgroup
 //              works while the tensor core serves the other.
 // Every wait is bounded (CB_DEVERR_TIMEOUT) and nothing spins forever.
+//
+// Sliding-window layers ("Continuous batching architecture", Memory
+// management): with window W > 0 query position p attends keys p-W+1..p.
+// A CTA then streams only the KV tiles from the one holding key
+// (first query of its pair) - W + 1; pages before that key read as zeros
+// (they may have been recycled), and keys before each row's window are
+// masked in the softmax like the causal upper triangle.  A row whose keys
+// in the tiles seen so far are all masked keeps a running max of -inf and
+// exponentiates against 0, so its weights stay exactly 0.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -109,6 +118,7 @@ struct Params {
   int32_t num_tokens;         // rows of q / out
   int32_t num_blocks, max_blocks_per_seq, num_q_heads, num_kv_heads, group;
   float scale_log2;
+  int32_t window;             // sliding window (0: full attention)
   uint32_t* error_word;
 };
 
@@ -182,6 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int last_tok = min(tok0 + 2 * tpt - 1, q_len - 1);
   const int n_tiles = (start + last_tok) / kBN + 1;
   const int npages = (L + kPage - 1) / kPage;
+  // with a window, the pair's first query reads keys from key_lo on: KV
+  // tiles j_lo .. n_tiles - 1 (nt of them; ring positions count from j_lo)
+  const int key_lo = p.window > 0 ? max(0, start + tok0 - p.window + 1) : 0;
+  const int j_lo = key_lo / kBN;
+  const int lo_pg = key_lo / kPage;
+  const int nt = n_tiles - j_lo;
 
   if (threadIdx.x == 0) {
     // a stage is free once every active MMA issuer (one per query tile)
@@ -229,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto page_row = [&](int j) -> int {
       const int page = j * (kBN / kPage) + lane;
       int row = oob_row;
-      if (lane < kBN / kPage && j < n_tiles && page < npages) {
+      if (lane < kBN / kPage && j < n_tiles && page < npages && page >= lo_pg) {
         const int blk = __ldg(p.block_tables + (int64_t)r * W + page);
         if (blk >= 0 && blk < p.num_blocks)
           row = (blk * p.num_kv_heads + g) * kPage;
@@ -238,16 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return row;
     };
-    int row_next = page_row(0);
+    int row_next = page_row(j_lo);
     int issued = 0;
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int jj = 0; jj < nt; ++jj) {
       const int row = row_next;
-      row_next = page_row(j + 1);  // in flight while we wait
-      const int s = j % nst;
+      row_next = page_row(j_lo + jj + 1);  // in flight while we wait
+      const int s = jj % nst;
       uint64_t* full = hv ? &B->v_full[s] : &B->k_full[s];
-      if (j >= nst) {
+      if (jj >= nst) {
         uint64_t* empty = hv ? &B->v_empty[s] : &B->k_empty[s];
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(empty, ((j / nst) - 1) & 1));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(empty, ((jj / nst) - 1) & 1));
         if (!ok) { abort_cta(B, p.error_word); break; }
       }
       if (*reinterpret_cast<volatile uint32_t*>(&B->abort)) break;
@@ -262,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      issued = j + 1;
+      issued = jj + 1;
     }
     // drain: every issued copy lands before the CTA may exit
     for (int j = (issued > nst ? issued - nst : 0); j < issued; ++j)
@@ -289,12 +305,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(smem + SmemLayout::v), kHalf, 1024);
       constexpr uint32_t kTileDesc = kTileBytes >> 4;
       bool ok = true;
-      for (int j = 0; j <= n_tiles && ok; ++j) {
-        if (j >= 1) {
-          const int jp = j - 1;
-          const int sp = jp % kStagesV;
-          ok = wait_or_abort(&B->p_full[t], jp & 1, B, p.error_word) &&
-               wait_or_abort(&B->v_full[sp], (jp / kStagesV) & 1, B, p.error_word);
+      for (int jj = 0; jj <= nt && ok; ++jj) {
+        if (jj >= 1) {
+          const int jr = jj - 1;            // ring position of the previous tile
+          const int jp = j_lo + jr;         // its KV tile
+          const int sp = jr % kStagesV;
+          ok = wait_or_abort(&B->p_full[t], jr & 1, B, p.error_word) &&
+               wait_or_abort(&B->v_full[sp], (jr / kStagesV) & 1, B, p.error_word);
           if (!ok) break;
           if ((L & (kPage - 1)) != 0 && jp == (L - 1) / kBN) {
             // rows L .. end of the last page hold pool slots past the
@@ -315,13 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             tc::mma_f16_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, bv + (kk * 2048 >> 4),
-                           idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+                           idesc_pv, (jr > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(&B->v_empty[sp]);
-          if (j == n_tiles) tc::mma_commit(&B->o_done[t]);
+          if (jj == nt) tc::mma_commit(&B->o_done[t]);
         }
-        if (j < n_tiles) {
-          const int s = j % kStagesK;
-          ok = wait_or_abort(&B->k_full[s], (j / kStagesK) & 1, B, p.error_word);
+        if (jj < nt) {
+          const int s = jj % kStagesK;
+          ok = wait_or_abort(&B->k_full[s], (jj / kStagesK) & 1, B, p.error_word);
           if (!ok) break;
           const uint64_t bk = dk0 + s * kTileDesc;
 #pragma unroll
@@ -365,21 +382,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     const float sl = p.scale_log2;
     bool ok = active;
-    for (int j = 0; j < n_tiles && ok; ++j) {
+    // keys before key_row are outside this row's window
+    const int key_row = p.window > 0 ? pos - p.window + 1 : -(1 << 30);
+    for (int jj = 0; jj < nt && ok; ++jj) {
       // the two warpgroups take turns (softmax 0 of tile j, softmax 1 of
       // tile j, softmax 0 of tile j + 1, ...), so each runs alone on the
       // SM's exp and FMA units while the tensor core works for the other
-      if (has_t1 && (t == 1 || j >= 1)) {
-        const bool tw = __all_sync(0xffffffffu, t == 0 ? mbar_wait(&B->p_full[1], (j - 1) & 1)
-                                                     : mbar_wait(&B->p_full[0], j & 1));
+      if (has_t1 && (t == 1 || jj >= 1)) {
+        const bool tw = __all_sync(0xffffffffu, t == 0 ? mbar_wait(&B->p_full[1], (jj - 1) & 1)
+                                                     : mbar_wait(&B->p_full[0], jj & 1));
         if (!tw) { abort_cta(B, p.error_word); ok = false; break; }
       }
-      bool w = __all_sync(0xffffffffu, mbar_wait(&B->s_full[t], j & 1));
+      bool w = __all_sync(0xffffffffu, mbar_wait(&B->s_full[t], jj & 1));
       if (!w) { abort_cta(B, p.error_word); ok = false; break; }
       tc::fence_after_sync();
-      const int kbase = j * kBN;
-      const int lim = pos - kbase;               // key kbase+i visible iff i <= lim
-      const bool masked = lim < kBN - 1;
+      const int kbase = (j_lo + jj) * kBN;
+      const int lim = pos - kbase;               // key kbase+i visible iff lo <= i <= lim
+      const int lo = key_row - kbase;
+      const bool masked = lim < kBN - 1 || lo > 0;
       // the whole S row in registers with one TMEM wait
       float sv[kBN];
 #pragma unroll
@@ -387,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_wait_ld();
       if (masked) {
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) sv[i] = (i <= lim) ? sv[i] : -INFINITY;
+        for (int i = 0; i < kBN; ++i) sv[i] = (i <= lim && i >= lo) ? sv[i] : -INFINITY;
       }
       // row max in 8 chains of 3-input max
       float mx[8];
@@ -411,7 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // in the bf16 layout the P.V MMA reads.  The row sum adds exactly those
       // bf16 values in fp32 (4 packed chains).  P is written over the S
       // columns (all read above).
-      const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(-m_use, -m_use);
+      // a row with every key so far masked has m_use = -inf: subtract 0
+      // instead, so its masked scores give 2^-inf = 0 rather than NaN
+      const float m_sub = m_use == -INFINITY ? 0.f : m_use;
+      const float2 sl2 = make_float2(sl, sl), nm2 = make_float2(-m_sub, -m_sub);
       float2 ls2[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) ls2[u] = make_float2(0.f, 0.f);
@@ -432,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run = l_run * alpha + lsum;
       // S_t(j) ready implies P_t.V(j-1) completed (same issuing thread, in
       // order), so O_t is stable here and may be rescaled.
-      if (j >= 1 && __any_sync(0xffffffffu, resc)) {
+      if (jj >= 1 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float o[32];
@@ -560,6 +583,7 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   p.num_kv_heads = a.num_kv_heads;
   p.group = G;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.window = a.sliding_window;
   p.error_word = error_word;
   const int tpp = 2 * (kBM / G);  // tokens per CTA (a pair of query tiles)
   dim3 grid((a.max_q_len + tpp - 1) / tpp, a.num_kv_heads, a.num_reqs - a.num_decodes);

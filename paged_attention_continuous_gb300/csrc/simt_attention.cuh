@@ -7,7 +7,8 @@
 // the specialised kernels do not cover.  Same definition as every other
 // path: "Chunked Prefill" (Ultralytics glossary), How chunked prefill works
 // -- query i of a row at absolute position p = seq_len - q_len + i attends
-// keys 0..p of its request.
+// keys 0..p of its request; with a sliding window W > 0 only keys
+// p-W+1..p ("Continuous batching architecture", Memory management).
 #pragma once
 
 #include <cstdint>
@@ -31,6 +32,7 @@ struct Params {
   int32_t num_blocks, max_blocks_per_seq, block_size;
   int32_t num_q_heads, num_kv_heads;
   float scale_log2;
+  int32_t window;               // sliding window (0: full attention)
   uint32_t* error_word;
 };
 
@@ -92,7 +94,8 @@ __global__ void __launch_bounds__(256) rows_kernel(const Params p) {
   const T* kc = static_cast<const T*>(p.k_cache);
   const T* vc = static_cast<const T*>(p.v_cache);
   const int npages = pos / bs + 1;
-  for (int pg = 0; pg < npages; ++pg) {
+  const int k_lo = p.window > 0 && pos + 1 > p.window ? pos + 1 - p.window : 0;
+  for (int pg = k_lo / bs; pg < npages; ++pg) {
     const int blk = p.block_tables[(int64_t)r * p.max_blocks_per_seq + pg];
     if (blk < 0 || blk >= p.num_blocks) {
       if (lane == 0) set_error(p.error_word, CB_DEVERR_BLOCK_RANGE);
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(256) rows_kernel(const Params p) {
     }
     const int64_t page_off = ((int64_t)blk * p.num_kv_heads + g) * bs * D;
     const int nk = min(bs, pos + 1 - pg * bs);
-    for (int i = 0; i < nk; ++i) {
+    for (int i = max(0, k_lo - pg * bs); i < nk; ++i) {
       const T* krow = kc + page_off + (int64_t)i * D + lane * kDPL;
       const T* vrow = vc + page_off + (int64_t)i * D + lane * kDPL;
       float dot = 0.f;

@@ -115,13 +115,15 @@ class StepRunner:
     def __init__(self, *, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  dtype: str, max_reqs: int, max_tokens: int, max_blocks_per_seq: int,
                  num_layers: int = 1, block_size: int = 16, device: str = "cuda",
-                 scale: Optional[float] = None, zero_cache: bool = True, swap_blocks: int = 0):
+                 scale: Optional[float] = None, zero_cache: bool = True, swap_blocks: int = 0,
+                 sliding_window: int = 0):
         import torch
         self.torch = torch
         self.dt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
         self.Hq, self.Hkv, self.D = num_q_heads, num_kv_heads, head_dim
         self.block_size = block_size
         self.num_blocks = num_blocks
+        self.sliding_window = int(sliding_window)
         self.max_reqs, self.max_tokens = max_reqs, max_tokens
         self.W = max_blocks_per_seq
         self.scale = 1.0 / math.sqrt(head_dim) if scale is None else scale
@@ -194,7 +196,8 @@ class StepRunner:
         return paged_attention(q, kc, vc, ds.cu_seqlens_q, ds.seq_lens, ds.block_tables,
                                num_decodes=ds.num_decodes, max_q_len=ds.max_q_len,
                                max_seq_len=ds.max_seq_len, scale=self.scale,
-                               workspace=self.workspace, out=out)
+                               workspace=self.workspace, out=out,
+                               sliding_window=self.sliding_window)
 
 
 def bucket(n: int, lo: int = 1) -> int:
@@ -230,13 +233,15 @@ class GraphStepRunner:
     def __init__(self, *, num_blocks: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                  dtype: str, max_reqs: int, max_tokens: int, max_blocks_per_seq: int,
                  num_layers: int = 1, block_size: int = 16, device: str = "cuda",
-                 scale: Optional[float] = None, zero_cache: bool = True, swap_blocks: int = 0):
+                 scale: Optional[float] = None, zero_cache: bool = True, swap_blocks: int = 0,
+                 sliding_window: int = 0):
         import torch
         self.torch = torch
         self.dt = {"bf16": torch.bfloat16, "f32": torch.float32}[dtype]
         self.Hq, self.Hkv, self.D = num_q_heads, num_kv_heads, head_dim
         self.block_size = block_size
         self.W = max_blocks_per_seq
+        self.sliding_window = int(sliding_window)
         self.L = num_layers
         self.scale = 1.0 / math.sqrt(head_dim) if scale is None else scale
         self.R_cap = 2 * bucket(max_reqs)     # padded decode rows + padded prefill rows
@@ -326,7 +331,7 @@ class GraphStepRunner:
                             max_q_len=min(max(mqb, 1), W * self.block_size),
                             max_seq_len=W * self.block_size,
                             scale=self.scale, workspace=self.workspace,
-                            out=self.out_buf[layer][:Tb])
+                            out=self.out_buf[layer][:Tb], sliding_window=self.sliding_window)
 
     def run(self, key):
         """Run the step last prepared (key from prepare)."""

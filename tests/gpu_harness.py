@@ -60,7 +60,7 @@ class ParityRun:
                                  max_tokens=max_tokens or sc.max_batch_tokens,
                                  max_blocks_per_seq=sc.max_blocks_per_seq,
                                  num_layers=sc.num_layers, device=device,
-                                 swap_blocks=sc.swap_blocks)
+                                 swap_blocks=sc.swap_blocks, sliding_window=sc.sliding_window)
         self.device = device
         self.pristine = []
         for layer in range(sc.num_layers):
@@ -181,7 +181,8 @@ class ParityRun:
                     if b >= 0:
                         bt[j, c] = self.idx[int(b)]
             ref = oatt.paged_attention(qo, self.sub_k[layer], self.sub_v[layer], np.asarray(cu),
-                                       so["seq_lens"][rows], bt, bs, sc.softmax_scale)
+                                       so["seq_lens"][rows], bt, bs, sc.softmax_scale,
+                                       window=sc.sliding_window)
             ref_outs.append(ref)
         assert self.o.step_done() == self.c.step_done()
         errs = self.runner.workspace.read_errors()

@@ -275,6 +275,27 @@ def shared_prefix(seed: int = 0, num_requests: int = 48, num_system: int = 4,
         prefix_caching=True)
 
 
+def sliding_trace(seed: int = 0, num_requests: int = 32, window: int = 384,
+                  num_blocks: int = 512, num_layers: int = 2) -> Scenario:
+    """A model whose layers all use a sliding window of 384 tokens: prompts
+    U[64, 1500], outputs U[8, 200], arrivals over the first 10 steps, 32 Q /
+    8 KV heads, D = 128, bf16, budget 1024 tokens, a 512-block pool (8,192
+    tokens) that only fits the traffic because pages out of the window are
+    recycled."""
+    rng = np.random.default_rng(seed)
+    waiting = [WaitingRequest(req_id=i, prompt_len=int(rng.integers(64, 1500, endpoint=True)),
+                              output_len=int(rng.integers(8, 200, endpoint=True)),
+                              arrival_step=int(rng.integers(0, 10)))
+               for i in range(num_requests)]
+    waiting.sort(key=lambda w: w.arrival_step)
+    return Scenario(
+        name="sliding_trace", num_q_heads=32, num_kv_heads=8, head_dim=128, dtype="bf16",
+        num_blocks=num_blocks, max_batch_tokens=1024, max_requests_per_batch=32,
+        max_prefill_chunk=0, safety_margin=0.0, max_blocks_per_seq=0,
+        free_list=permuted_free_list(num_blocks, seed + 1), running=[], waiting=waiting,
+        num_layers=num_layers, value_scale=1.0, seed=seed, sliding_window=window)
+
+
 SCENARIOS = {
     "chunked_prefill_1000": chunked_prefill_1000,
     "decode_64": decode_64,
@@ -284,6 +305,7 @@ SCENARIOS = {
     "prefill_chunk_16k": prefill_chunk_16k,
     "offload_pressure": offload_pressure,
     "shared_prefix": shared_prefix,
+    "sliding_trace": sliding_trace,
 }
 
 

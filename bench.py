@@ -117,17 +117,21 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------- work models
-def decode_bytes(step, Hq, Hkv, D, elem):
-    """Algorithmic bytes of the decode rows: each cached K and V row read once
-    per KV head, plus q read and out written."""
+def decode_bytes(step, Hq, Hkv, D, elem, window=0):
+    """Algorithmic bytes of the decode rows: each K and V row the query sees
+    (all of them, or the last ``window``) read once per KV head, plus q read
+    and out written."""
     nd = step["num_decodes"]
     seq = np.asarray(step["seq_lens"][:nd], dtype=np.int64)
+    if window > 0:
+        seq = np.minimum(seq, window)
     return int(seq.sum() * Hkv * D * 2 * elem + nd * Hq * D * 2 * elem)
 
 
-def prefill_flops(step, Hq, D):
+def prefill_flops(step, Hq, D, window=0):
     """Algorithmic FLOPs of the prefill rows: 2*D for q.k and 2*D for p.v per
-    unmasked (query, key) pair and query head."""
+    unmasked (query, key) pair and query head (query position p sees p + 1
+    keys, or min(p + 1, window))."""
     nd = step["num_decodes"]
     cu = np.asarray(step["cu_seqlens_q"], dtype=np.int64)
     seq = np.asarray(step["seq_lens"], dtype=np.int64)
@@ -135,7 +139,10 @@ def prefill_flops(step, Hq, D):
     for r in range(nd, step["num_reqs"]):
         n = int(cu[r + 1] - cu[r])
         start = int(seq[r]) - n
-        pairs += n * start + n * (n + 1) // 2
+        if window > 0:
+            pairs += int(np.minimum(np.arange(start + 1, start + n + 1), window).sum())
+        else:
+            pairs += n * start + n * (n + 1) // 2
     return int(4 * D * Hq * pairs)
 
 
@@ -348,35 +355,52 @@ def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
             "sampled_steps": per_step, "reps_per_step": reps}
 
 
-def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000, graphs=False):
-    """Request trace: 2,000 requests with Poisson(20) arrivals per step and
-    lognormal prompt / output lengths (medians 512 / 128), 4 layers each with
-    its own 65,536-block pool, budget 8,192 tokens and 256 requests per step,
-    run until every request has finished.  Per step: the host scheduler call
-    (timed on the host), one metadata upload, and per layer the step's fresh
-    q/k/v (drawn per (step, layer), untimed) then append + attention (timed
-    with CUDA events).  Reports whole-trace tokens/s, the additive roofline
-    fraction (decode bytes / HBM peak + prefill FLOPs / tensor peak, over the
-    measured kernel time) and the KV-block fragmentation (slots allocated but
-    not yet holding a token, over all allocated slots, mean over steps).
-    With ``graphs`` every step (all layers) is one CUDA-graph replay of its
-    padded bucket (GraphStepRunner); q/k/v are copied into its static
-    buffers outside the timed replay."""
+TRACE_DESC = "trace_2000 (2,000 requests, Poisson(20) arrivals, lognormal lengths, " \
+             "4 layers x 65,536 blocks, 32Q/8KV, D=128, budget 8192 / 256 reqs)"
+
+
+def scheduler_for(cb, sc):
+    """The C scheduler configured from every option a workload sets."""
+    return cb.Scheduler(block_size=sc.block_size, num_blocks=sc.num_blocks,
+                        max_batch_tokens=sc.max_batch_tokens,
+                        max_requests_per_batch=sc.max_requests_per_batch,
+                        max_blocks_per_seq=sc.max_blocks_per_seq,
+                        max_prefill_chunk=sc.max_prefill_chunk, safety_margin=sc.safety_margin,
+                        free_list=sc.free_list, policy=sc.policy, offload=sc.offload,
+                        swap_blocks=sc.swap_blocks, prefix_caching=sc.prefix_caching,
+                        sliding_window=sc.sliding_window)
+
+
+def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000, graphs=False, sc=None,
+                  desc=TRACE_DESC):
+    """A request trace run until every request has finished (by default the
+    2,000-request trace: Poisson(20) arrivals per step, lognormal prompt /
+    output lengths with medians 512 / 128, 4 layers each with its own
+    65,536-block pool, budget 8,192 tokens and 256 requests per step).  Per
+    step: the host scheduler call (timed on the host), the step's offload
+    swaps and metadata upload (timed with CUDA events when the step has
+    swaps), and per layer the step's fresh q/k/v (drawn per (step, layer),
+    untimed) then append + attention (timed with CUDA events).  Reports
+    whole-trace tokens/s, the additive roofline fraction (decode bytes / HBM
+    peak + prefill FLOPs / tensor peak, over the measured kernel time) and
+    the KV-block fragmentation (slots allocated but not yet holding a token,
+    over all allocated slots, mean over steps).  With ``graphs`` every step
+    (all layers) is one CUDA-graph replay of its padded bucket
+    (GraphStepRunner); q/k/v are copied into its static buffers outside the
+    timed replay."""
     from paged_attention_continuous_gb300.step import GraphStepRunner, StepRunner
-    sc = workloads.trace_2000()
-    s = cb.Scheduler(block_size=sc.block_size, num_blocks=sc.num_blocks,
-                     max_batch_tokens=sc.max_batch_tokens,
-                     max_requests_per_batch=sc.max_requests_per_batch,
-                     max_blocks_per_seq=sc.max_blocks_per_seq,
-                     max_prefill_chunk=sc.max_prefill_chunk, safety_margin=sc.safety_margin,
-                     free_list=sc.free_list)
+    sc = workloads.trace_2000() if sc is None else sc
+    s = scheduler_for(cb, sc)
     Runner = GraphStepRunner if graphs else StepRunner
     runner = Runner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
                     num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim, dtype=sc.dtype,
                     max_reqs=sc.max_requests_per_batch, max_tokens=sc.max_batch_tokens,
                     max_blocks_per_seq=sc.max_blocks_per_seq, num_layers=sc.num_layers,
-                    device=dev)
+                    device=dev, swap_blocks=sc.swap_blocks, sliding_window=sc.sliding_window)
+    W = sc.sliding_window
     events = []
+    swap_events = []
+    swap_bytes = 0
     t_host = 0.0
     tokens = 0
     d_bytes = 0
@@ -389,20 +413,39 @@ def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000, graphs=False):
     while finished < len(sc.waiting) and step < max_steps:
         while nxt < len(sc.waiting) and sc.waiting[nxt].arrival_step <= step:
             w = sc.waiting[nxt]
-            s.add_request(w.req_id, w.prompt_len, w.output_len)
+            if w.tokens is not None:
+                s.add_request(w.req_id, w.prompt_len, w.output_len, tokens=w.tokens)
+            else:
+                s.add_request(w.req_id, w.prompt_len, w.output_len)
             nxt += 1
         h0 = time.perf_counter()
         st = s.schedule_step()
         t_host += time.perf_counter() - h0
+        has_swaps = len(st["swap_in"]) + len(st["swap_out"]) > 0
+        if has_swaps:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
         if st["status"] != 0 or st["num_reqs"] == 0:
+            swap_bytes += runner.apply_swaps(st)
+            if has_swaps:
+                e1.record()
+                swap_events.append((e0, e1))
+            if st["status"] == 0:
+                s.step_done()
             stalled_steps += 1
             step += 1
             continue
         T = st["num_tokens"]
+        if has_swaps:
+            swap_bytes += (len(st["swap_in"]) + len(st["swap_out"])) * runner.swap.block_bytes * \
+                2 * sc.num_layers
         if graphs:
             key, _ = runner.prepare(st)
         else:
             ds = runner.upload(st)
+        if has_swaps:
+            e1.record()
+            swap_events.append((e0, e1))
         for layer in range(sc.num_layers):
             sd = [workloads.step_seed(sc.seed, step, layer, c) for c in range(3)]
             q = workloads.token_tensors(T, sc.num_q_heads, sc.head_dim, seed=sd[0], dtype=sc.dtype,
@@ -431,22 +474,37 @@ def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000, graphs=False):
         finished += len(s.step_done())
         t_host += time.perf_counter() - h0
         tokens += T
-        d_bytes += sc.num_layers * decode_bytes(st, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, 2)
-        p_flops += sc.num_layers * prefill_flops(st, sc.num_q_heads, sc.head_dim)
+        d_bytes += sc.num_layers * decode_bytes(st, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, 2,
+                                                W)
+        p_flops += sc.num_layers * prefill_flops(st, sc.num_q_heads, sc.head_dim, W)
         sl = np.asarray(st["seq_lens"], dtype=np.int64)
         alloc = ((sl + sc.block_size - 1) // sc.block_size) * sc.block_size
         frag.append(float((alloc - sl).sum() / max(alloc.sum(), 1)))
         step += 1
     torch.cuda.synchronize()
     t_dev = sum(a.elapsed_time(b) for a, b in events) / 1e3
+    t_swap = sum(a.elapsed_time(b) for a, b in swap_events) / 1e3
     assert runner.workspace.read_errors() == 0
+    if runner.swap is not None:
+        assert runner.swap.read_errors() == 0
     n_graphs = len(runner.graphs) if graphs else 0
+    hits = s.prefix_stats()[0]
     del runner
     torch.cuda.empty_cache()
     t_roof = d_bytes / (hbm * 1e9) + p_flops / (bf16 * 1e12)
+    extra = {}
+    if sc.offload:
+        # the swaps of this small trace are a few blocks per step: their
+        # region time is launch latency; the bandwidth is measure_swap's
+        extra["offload"] = {"swap_bytes": int(swap_bytes), "steps_with_swaps": len(swap_events),
+                            "ms_swap_and_upload_regions": round(t_swap * 1e3, 3)}
+    if sc.prefix_caching:
+        extra["prefix_hit_tokens"] = int(hits)
+        extra["prompt_tokens"] = int(sum(w.prompt_len for w in sc.waiting))
+    if W:
+        extra["sliding_window"] = W
     return {"graphs": n_graphs if graphs else None,
-            "workload": "trace_2000 (2,000 requests, Poisson(20) arrivals, lognormal lengths, "
-                        "4 layers x 65,536 blocks, 32Q/8KV, D=128, budget 8192 / 256 reqs)",
+            "workload": desc, **extra,
             "steps": step, "steps_without_batch": stalled_steps, "finished": finished,
             "tokens": int(tokens),
             "tokens_per_s_device": round(tokens / t_dev, 1) if t_dev else 0.0,
@@ -457,6 +515,104 @@ def measure_trace(cb, torch, dev, hbm, bf16, max_steps=20000, graphs=False):
             "fragmentation_mean": round(float(np.mean(frag)) if frag else 0.0, 4),
             "timed": "per layer: cb_kv_append + cb_paged_attention (CUDA events); "
                      "scheduler calls on the host; q/k/v generation untimed"}
+
+
+def measure_swap(cb, torch, dev, reps=5):
+    """cb_kv_swap over the CPU-GPU link: 256 blocks of every layer's K and V
+    of a 32-layer model (8 KV heads x 16 tokens x 128 dims bf16 = 32 KB per
+    block and pool, 64 pools: 512 MiB per direction) moved from the device
+    caches to the pinned swap pool and back, against one contiguous
+    cudaMemcpyAsync of the same byte count (the copy engine) each way."""
+    layers, nb, n = 32, 512, 256
+    shape = (8, 16, 128)
+    devp = [torch.empty((nb,) + shape, dtype=torch.bfloat16, device=dev) for _ in range(2 * layers)]
+    hostp = [torch.empty((n,) + shape, dtype=torch.bfloat16, pin_memory=True)
+             for _ in range(2 * layers)]
+    blocks = torch.randperm(nb, device=dev)[:n].to(torch.int32)
+    slots = torch.arange(n, dtype=torch.int32, device=dev)
+    ew = torch.zeros(1, dtype=torch.int32, device=dev)
+    nbytes = n * 2 * layers * devp[0][0].numel() * 2
+    stream = torch.cuda.current_stream()
+    out = lambda: cb.kv_swap(devp, hostp, blocks, slots, error_word=ew)
+    back = lambda: cb.kv_swap(hostp, devp, slots, blocks, error_word=ew)
+    hbuf = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d2h = lambda: hbuf.copy_(dbuf, non_blocking=True)
+    h2d = lambda: dbuf.copy_(hbuf, non_blocking=True)
+    res = {}
+    for name, f in (("swap_out", out), ("swap_in", back), ("memcpy_d2h", d2h), ("memcpy_h2d", h2d)):
+        f()
+        t = time_each(torch, f, reps, stream) / reps
+        res[name + "_gbs"] = round(nbytes / t / 1e9, 1)
+    torch.cuda.synchronize()
+    assert int(ew.item()) == 0
+    del devp, hostp, hbuf, dbuf
+    torch.cuda.empty_cache()
+    return {"kernel": "kv_swap_kernel", "bytes_per_direction": int(nbytes),
+            "workload": "256 blocks x 64 pools (32 layers K and V, 32 KB blocks)", **res,
+            "frac_of_memcpy_out": round(res["swap_out_gbs"] / res["memcpy_d2h_gbs"], 3),
+            "frac_of_memcpy_in": round(res["swap_in_gbs"] / res["memcpy_h2d_gbs"], 3),
+            "launches_timed": reps}
+
+
+def measure_window_decode(cb, torch, dev, reps, hbm):
+    """Decode on sliding-window layers: 256 requests with contexts
+    U[2048, 32768] attending the last 4,096 tokens (32 Q / 8 KV heads,
+    D = 128, bf16); block tables hold -1 before each window (recycled
+    pages), so only window pages exist.  Decode kernel GB/s vs HBM peak."""
+    rng = np.random.default_rng(7)
+    R, W, Hq, Hkv, D = 256, 4096, 32, 8, 128
+    L = rng.integers(2048, 32768, size=R, endpoint=True)
+    first = np.maximum(L - W, 0) // 16
+    pages = (L + 15) // 16
+    nb = int((pages - first).sum())
+    perm = rng.permutation(nb).astype(np.int32)
+    Wmax = int(pages.max())
+    bt = np.full((R, Wmax), -1, dtype=np.int32)
+    o = 0
+    for r in range(R):
+        k = int(pages[r] - first[r])
+        bt[r, first[r]:pages[r]] = perm[o:o + k]
+        o += k
+    kc = workloads.cache_fill(nb, Hkv, 16, D, seed=31, dtype="bf16", scale=0.5, device=dev)
+    vc = workloads.cache_fill(nb, Hkv, 16, D, seed=32, dtype="bf16", scale=0.5, device=dev)
+    q = workloads.token_tensors(R, Hq, D, seed=33, dtype="bf16", scale=0.5, device=dev)
+    out = torch.empty_like(q)
+    ws = cb.Workspace(R, Hq, Hkv, D, device=dev)
+    cu = torch.arange(R + 1, dtype=torch.int32, device=dev)
+    sl = torch.from_numpy(L.astype(np.int32)).to(dev)
+    btd = torch.from_numpy(bt).to(dev)
+    f = lambda: cb.paged_attention(q, kc, vc, cu, sl, btd, num_decodes=R, max_q_len=1,
+                                   max_seq_len=int(L.max()), scale=1 / math.sqrt(D), workspace=ws,
+                                   out=out, sliding_window=W)
+    for _ in range(5):
+        f()
+    t = time_each(torch, f, reps, torch.cuda.current_stream()) / reps
+    assert ws.read_errors() == 0
+    nbytes = decode_bytes({"num_decodes": R, "seq_lens": L}, Hq, Hkv, D, 2, W)
+    gbs = nbytes / t / 1e9
+    del kc, vc, ws
+    torch.cuda.empty_cache()
+    return {"workload": "256 decodes, ctx U[2048,32768], window 4096, 32Q/8KV, D=128",
+            "kernel": "decode_kernel (window)", "achieved_gbs": round(gbs, 1), "peak_gbs": hbm,
+            "frac": round(gbs / hbm, 4), "ms_per_launch": round(t * 1e3, 4),
+            "algorithmic_bytes_per_launch": int(nbytes), "launches_timed": reps}
+
+
+def measure_prefix(cb, torch, dev, hbm, bf16):
+    """The shared-system-prompt trace (48 requests over 4 system prompts of
+    U[200, 1200] tokens plus U[16, 400]-token suffixes, 2 layers) with and
+    without prefix caching: device time for the whole trace and the prompt
+    tokens that were reused instead of recomputed."""
+    import dataclasses
+    sc = workloads.shared_prefix(0)
+    desc = "shared_prefix (48 requests, 4 shared system prompts, 2 layers, 32Q/8KV)"
+    on = measure_trace(cb, torch, dev, hbm, bf16, sc=sc, desc=desc)
+    off = measure_trace(cb, torch, dev, hbm, bf16,
+                        sc=dataclasses.replace(sc, prefix_caching=False), desc=desc)
+    return {"workload": desc, "with_prefix_caching": on, "without": off,
+            "device_time_ratio": round(off["ms_device_total"] / on["ms_device_total"], 3)
+            if on["ms_device_total"] else None}
 
 
 # ----------------------------------------------------------- CPU oracle
@@ -679,6 +835,17 @@ def run_ours(args, rank, world):
         line["long_prompt"] = measure_long_prompt(cb, torch, dev, 3, hbm, bf16, bf16s)
         line["trace"] = measure_trace(cb, torch, dev, hbm, bf16)
         line["trace_graphs"] = measure_trace(cb, torch, dev, hbm, bf16, graphs=True)
+        line["offload"] = {
+            "swap": measure_swap(cb, torch, dev),
+            "trace": measure_trace(cb, torch, dev, hbm, bf16, sc=workloads.offload_pressure(0),
+                                   desc="offload_pressure (24 requests, 40-block pool, 8-block "
+                                        "swap pool, 2 layers, 16Q/4KV)")}
+        line["prefix_caching"] = measure_prefix(cb, torch, dev, hbm, bf16)
+        line["sliding_window"] = {
+            "decode": measure_window_decode(cb, torch, dev, max(K, 20), hbm),
+            "trace": measure_trace(cb, torch, dev, hbm, bf16, sc=workloads.sliding_trace(0),
+                                   desc="sliding_trace (32 requests, window 384, 512-block "
+                                        "pool, 2 layers, 32Q/8KV)")}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sc, step, runner, q, k, v, torch, dev,
                                             budget_s=args.cpu_seconds)

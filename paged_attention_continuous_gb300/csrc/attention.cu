@@ -69,13 +69,13 @@ constexpr int decode_warps() {
   return sizeof(WS) * 8 + decode::kPlanSmemBytes <= 200 * 1024 ? 8 : 4;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool kWindow>
 cb_status launch_decode(const cb_attention_args& a, const WsLayout& L, cudaStream_t stream) {
   constexpr int kStages = 2;
   constexpr int kWarps = decode_warps<T, D, G>();
   using WS = decode::WarpSmem<T, D, G, kStages>;
   const size_t smem = sizeof(WS) * kWarps + decode::kPlanSmemBytes;
-  auto kern = decode::decode_kernel<T, D, G, kWarps, kStages>;
+  auto kern = decode::decode_kernel<T, D, G, kWarps, kStages, kWindow>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {
@@ -121,8 +121,10 @@ cb_status launch_decode(const cb_attention_args& a, const WsLayout& L, cudaStrea
 template <typename T>
 cb_status dispatch_decode(const cb_attention_args& a, const WsLayout& L, cudaStream_t s) {
   const int G = a.num_q_heads / a.num_kv_heads;
-#define CB_DEC(DD, GG) \
-  if (a.head_dim == DD && G == GG) return launch_decode<T, DD, GG>(a, L, s);
+#define CB_DEC(DD, GG)                                                               \
+  if (a.head_dim == DD && G == GG)                                                   \
+    return a.sliding_window > 0 ? launch_decode<T, DD, GG, true>(a, L, s)            \
+                                : launch_decode<T, DD, GG, false>(a, L, s);
   CB_DEC(128, 1) CB_DEC(128, 2) CB_DEC(128, 4) CB_DEC(128, 8)
   CB_DEC(64, 1) CB_DEC(64, 2) CB_DEC(64, 4) CB_DEC(64, 8)
 #undef CB_DEC

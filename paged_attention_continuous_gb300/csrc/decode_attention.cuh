@@ -200,7 +200,9 @@ __device__ __forceinline__ void store_row(T* row, int j, const float* v) {
   }
 }
 
-template <typename T, int D, int G, int kWarps, int kStages>
+// kWindow: the launch has a sliding window (p.window > 0); the full-attention
+// instantiation compiles the window arithmetic away.
+template <typename T, int D, int G, int kWarps, int kStages, bool kWindow>
 __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) {
   using C = Cfg<T, D, G>;
   using WS = WarpSmem<T, D, G, kStages>;
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
   const int Hkv = p.num_kv_heads;
   const int Hq = p.num_q_heads;
   const int W = p.max_blocks_per_seq;
+  const int win = kWindow ? p.window : 0;
 
   // ---- plan: pages per row -> split sizes -> prefixes of split counts -----
   // Rows are checked once here and kept in shared memory; a row that fails a
@@ -244,7 +247,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
         if (blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_DECODE_QLEN);
       }
     }
-    pages = (L + kPageTokens - 1) / kPageTokens - first_page(L, p.window);
+    pages = (L + kPageTokens - 1) / kPageTokens - first_page(L, win);
     row_len[i] = L;
     row_tok[i] = q0;
     my_pages += pages;
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
     for (int i = b; i < e; ++i) {
       const int Li = row_len[i];
       const RowSplit rs =
-          row_split((Li + kPageTokens - 1) / kPageTokens - first_page(Li, p.window), spa0, spb0);
+          row_split((Li + kPageTokens - 1) / kPageTokens - first_page(Li, win), spa0, spb0);
       const int na = rs.na, nb = rs.nb;
       plan_a[i + 1] = na;
       plan_b[i + 1] = nb;
@@ -416,7 +419,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
       const int r = p.row_begin + i;
       const int L = row_len[i];
       const int pages = (L + kPageTokens - 1) / kPageTokens;
-      const int fp = first_page(L, p.window);
+      const int fp = first_page(L, win);
       const int na = a1 - a0;
       const int bp = fp + na * spa0;
       nx_ok = true;
@@ -579,7 +582,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
       // keys [lo_t, valid) of this page are read: the sequence end on the
       // last page, the window start on the first
       const int valid = min(kPageTokens, d.seq_len - page * kPageTokens);
-      const int lo_t = first_key(d.seq_len, p.window) - page * kPageTokens;
+      const int lo_t = first_key(d.seq_len, win) - page * kPageTokens;
       const uint8_t* kp = ws.kv[st][0];
       const uint8_t* vp = ws.kv[st][1];
 

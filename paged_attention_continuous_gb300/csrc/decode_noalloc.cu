@@ -78,14 +78,14 @@ cb_status scratch_for_current_device(uint8_t** out) {
   return CB_OK;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool kWindow>
 cb_status launch(const cb_attention_args& a, uint8_t* scratch, const NoAllocLayout& L,
                  uint32_t* error_word, cudaStream_t stream) {
   constexpr int kStages = 2;
   using WS8 = decode::WarpSmem<T, D, G, kStages>;
   constexpr int kWarps = sizeof(WS8) * 8 + decode::kPlanSmemBytes <= 200 * 1024 ? 8 : 4;
   const size_t smem = sizeof(WS8) * kWarps + decode::kPlanSmemBytes;
-  auto kern = decode::decode_kernel<T, D, G, kWarps, kStages>;
+  auto kern = decode::decode_kernel<T, D, G, kWarps, kStages, kWindow>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return fail(CB_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
   int dev = 0, sms = 0;
@@ -126,8 +126,10 @@ template <typename T>
 cb_status dispatch(const cb_attention_args& a, uint8_t* s, const NoAllocLayout& L, uint32_t* ew,
                    cudaStream_t st) {
   const int G = a.num_q_heads / a.num_kv_heads;
-#define CB_NA(DD, GG) \
-  if (a.head_dim == DD && G == GG) return launch<T, DD, GG>(a, s, L, ew, st);
+#define CB_NA(DD, GG)                                                   \
+  if (a.head_dim == DD && G == GG)                                      \
+    return a.sliding_window > 0 ? launch<T, DD, GG, true>(a, s, L, ew, st) \
+                                : launch<T, DD, GG, false>(a, s, L, ew, st);
   CB_NA(128, 1) CB_NA(128, 2) CB_NA(128, 4) CB_NA(128, 8)
   CB_NA(64, 1) CB_NA(64, 2) CB_NA(64, 4) CB_NA(64, 8)
 #undef CB_NA

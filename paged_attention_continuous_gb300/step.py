@@ -152,12 +152,10 @@ class StepRunner:
             return 0
         return self.swap.apply(step)
 
-    def upload(self, step: dict, stream=None) -> DeviceStep:
-        """Queue the step's swaps, then copy its metadata to the device (one
-        pinned copy on the current stream).  The returned arrays stay valid
-        until the next upload on this runner; kernels that use them must be
-        queued on the same stream before that next upload."""
-        self.apply_swaps(step)
+    def _pack(self, step: dict, h: np.ndarray):
+        """Write the step's metadata into the host int32 buffer ``h`` (one
+        packed run: cu_seqlens_q, seq_lens, block_tables, slot_mapping);
+        returns (words, offsets)."""
         R, T = int(step["num_reqs"]), int(step["num_tokens"])
         if R > self.max_reqs or T > self.max_tokens:
             raise ValueError("step larger than the runner was sized for")
@@ -165,28 +163,40 @@ class StepRunner:
         bt = np.asarray(step["block_tables"], dtype=np.int32).reshape(R, -1)
         if bt.shape[1] != W:
             raise ValueError("block_tables width differs from max_blocks_per_seq")
-        n = (R + 1) + R + R * W + T
-        b = self._turn
-        self._turn ^= 1
-        if self._copied[b] is not None:
-            self._copied[b].synchronize()
-        h = self._host[b].numpy()
-        o = 0
-        h[o:o + R + 1] = step["cu_seqlens_q"]; o1 = o + R + 1
-        h[o1:o1 + R] = step["seq_lens"]; o2 = o1 + R
-        h[o2:o2 + R * W] = bt.reshape(-1); o3 = o2 + R * W
+        o1 = R + 1
+        o2 = o1 + R
+        o3 = o2 + R * W
+        h[0:o1] = step["cu_seqlens_q"]
+        h[o1:o2] = step["seq_lens"]
+        h[o2:o3] = bt.reshape(-1)
         h[o3:o3 + T] = step["slot_mapping"]
-        self._dev[:n].copy_(self._host[b][:n], non_blocking=True)
-        ev = self.torch.cuda.Event()
-        ev.record()
-        self._copied[b] = ev
-        d = self._dev
+        return o3 + T, (o1, o2, o3)
+
+    def _device_step(self, step: dict, d, n: int, offs) -> DeviceStep:
+        R, T, W = int(step["num_reqs"]), int(step["num_tokens"]), self.W
+        o1, o2, o3 = offs
         return DeviceStep(R, T, int(step["num_decodes"]), int(step["max_q_len"]) if "max_q_len" in step
                           else int(np.diff(step["cu_seqlens_q"]).max(initial=1)),
                           int(step["max_seq_len"]) if "max_seq_len" in step
                           else int(np.max(step["seq_lens"], initial=1)),
-                          d[0:R + 1], d[o1:o1 + R], d[o2:o2 + R * W].view(R, W), d[o3:o3 + T],
-                          4 * n)
+                          d[0:R + 1], d[o1:o2], d[o2:o3].view(R, W), d[o3:o3 + T], 4 * n)
+
+    def upload(self, step: dict, stream=None) -> DeviceStep:
+        """Queue the step's swaps, then copy its metadata to the device (one
+        pinned copy on the current stream).  The returned arrays stay valid
+        until the next upload on this runner; kernels that use them must be
+        queued on the same stream before that next upload."""
+        self.apply_swaps(step)
+        b = self._turn
+        self._turn ^= 1
+        if self._copied[b] is not None:
+            self._copied[b].synchronize()
+        n, offs = self._pack(step, self._host[b].numpy())
+        self._dev[:n].copy_(self._host[b][:n], non_blocking=True)
+        ev = self.torch.cuda.Event()
+        ev.record()
+        self._copied[b] = ev
+        return self._device_step(step, self._dev, n, offs)
 
     def run(self, ds: DeviceStep, q, k_new, v_new, layer: int = 0, out=None):
         """Append this step's K/V for ``layer`` and attend.  q [T, Hq, D],
@@ -198,6 +208,100 @@ class StepRunner:
                                max_seq_len=ds.max_seq_len, scale=self.scale,
                                workspace=self.workspace, out=out,
                                sliding_window=self.sliding_window)
+
+
+class PipelinedStepRunner(StepRunner):
+    """Async double-buffered batching ("Continuous batching architecture",
+    Async batching): two sets of input/output buffers and separate streams
+    for input copies, compute and output copies, so that while the device
+    computes step N, step N+1's inputs are copied in and step N-1's output is
+    copied out, and the host is free to schedule.
+
+    ``submit(step, q, k, v, out)`` takes the step's inputs in pinned host
+    memory -- per layer lists of q [T, Hq, D] and k/v [T, Hkv, D] (a single
+    tensor for one layer) -- and a pinned host ``out`` (per layer list, or
+    one tensor) that receives the attention output; it returns an event that
+    completes once ``out`` holds the result.  The caller leaves the input
+    tensors unchanged, and reads ``out`` only, after that event.  Steps use
+    the two buffer sets in turn: a set's inputs are refilled only after the
+    compute that read them (two steps back) finished, its output buffer is
+    rewritten only after the copy-out that read it, and its host staging
+    buffer only after the copy-in that read it.  Caches, workspace and swap
+    pool are the StepRunner's; swaps run on the compute stream ahead of the
+    step's kernels.  ``upload``/``run`` (current stream) may be used on the
+    same runner only with the device synchronised in between.
+    """
+
+    def __init__(self, **kw):
+        super().__init__(**kw)
+        torch = self.torch
+        dev = self.k_cache[0].device
+        L = len(self.k_cache)
+        T = self.max_tokens
+        mk = lambda h: [torch.empty(T, h, self.D, dtype=self.dt, device=dev) for _ in range(L)]
+        words = self._dev.shape[0]
+        self._sets = [dict(q=mk(self.Hq), k=mk(self.Hkv), v=mk(self.Hkv), out=mk(self.Hq),
+                           meta=torch.empty(words, dtype=torch.int32, device=dev),
+                           stage=torch.empty(words, dtype=torch.int32, pin_memory=True))
+                      for _ in range(2)]
+        self.in_stream = torch.cuda.Stream(device=dev)
+        self.compute_stream = torch.cuda.Stream(device=dev)
+        self.out_stream = torch.cuda.Stream(device=dev)
+        self._copied_in = [None, None]   # per set: copy-in finished
+        self._computed = [None, None]    # per set: compute finished
+        self._copied_out = [None, None]  # per set: copy-out finished
+        self._slot = 0
+
+    def submit(self, step: dict, q, k, v, out):
+        torch = self.torch
+        as_list = lambda x: list(x) if isinstance(x, (list, tuple)) else [x]
+        q, k, v, out = as_list(q), as_list(k), as_list(v), as_list(out)
+        L = len(self.k_cache)
+        if not (len(q) == len(k) == len(v) == len(out) == L):
+            raise ValueError("one q/k/v/out tensor per layer expected")
+        T = int(step["num_tokens"])
+        i = self._slot
+        self._slot ^= 1
+        st = self._sets[i]
+        if self._copied_in[i] is not None:
+            self._copied_in[i].synchronize()    # the set's host staging is free
+        n, offs = self._pack(step, st["stage"].numpy())
+        ins, ks, outs = self.in_stream, self.compute_stream, self.out_stream
+        with torch.cuda.stream(ins):
+            if self._computed[i] is not None:
+                ins.wait_event(self._computed[i])
+            st["meta"][:n].copy_(st["stage"][:n], non_blocking=True)
+            for layer in range(L):
+                st["q"][layer][:T].copy_(q[layer], non_blocking=True)
+                st["k"][layer][:T].copy_(k[layer], non_blocking=True)
+                st["v"][layer][:T].copy_(v[layer], non_blocking=True)
+            copied_in = torch.cuda.Event()
+            copied_in.record(ins)
+        self._copied_in[i] = copied_in
+        ds = self._device_step(step, st["meta"], n, offs)
+        with torch.cuda.stream(ks):
+            ks.wait_event(copied_in)
+            if self._copied_out[i] is not None:
+                ks.wait_event(self._copied_out[i])
+            self.apply_swaps(step)
+            for layer in range(L):
+                self.run(ds, st["q"][layer][:T], st["k"][layer][:T], st["v"][layer][:T],
+                         layer=layer, out=st["out"][layer][:T])
+            computed = torch.cuda.Event()
+            computed.record(ks)
+        self._computed[i] = computed
+        with torch.cuda.stream(outs):
+            outs.wait_event(computed)
+            for layer in range(L):
+                out[layer].copy_(st["out"][layer][:T], non_blocking=True)
+            copied_out = torch.cuda.Event()
+            copied_out.record(outs)
+        self._copied_out[i] = copied_out
+        return copied_out
+
+    def synchronize(self):
+        for s_ in (self.in_stream, self.compute_stream, self.out_stream):
+            s_.synchronize()
 
 
 def bucket(n: int, lo: int = 1) -> int:

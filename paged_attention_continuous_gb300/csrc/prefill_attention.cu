@@ -539,6 +539,31 @@ cb_status make_cache_map(CUtensorMap* m, const void* base, int64_t rows) {
   if (r != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return CB_OK;
 }
+// Tensor maps depend only on the cache's base address and size, so the last
+// few are kept (a step calls the kernel once per layer, K and V each).
+cb_status cached_cache_map(CUtensorMap* m, const void* base, int64_t rows) {
+  struct Entry {
+    const void* base;
+    int64_t rows;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 64;
+  static Entry entries[kEntries];
+  static int used = 0, next = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (entries[i].base == base && entries[i].rows == rows) {
+      *m = entries[i].map;
+      return CB_OK;
+    }
+  cb_status st = make_cache_map(m, base, rows);
+  if (st != CB_OK) return st;
+  entries[next] = Entry{base, rows, *m};
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return CB_OK;
+}
 }  // namespace prefill
 
 bool prefill_supported(int group) {
@@ -564,9 +589,9 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * kPage;
   if (rows >= ((int64_t)1 << 31) - kPage) return CB_ERR_UNSUPPORTED;
   Params p{};
-  cb_status st = make_cache_map(&p.tmap_k, a.k_cache, rows);
+  cb_status st = cached_cache_map(&p.tmap_k, a.k_cache, rows);
   if (st != CB_OK) return st;
-  st = make_cache_map(&p.tmap_v, a.v_cache, rows);
+  st = cached_cache_map(&p.tmap_v, a.v_cache, rows);
   if (st != CB_OK) return st;
   p.k_cache = a.k_cache;
   p.v_cache = a.v_cache;

@@ -639,13 +639,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
 #pragma unroll
       for (int o = C::kLG; o < 32; o <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
       const float m_new = fmaxf(m_own, pm);
-      const float a_own = exp2f(m_own - m_new);
+      const float a_own = ex2_approx(m_own - m_new);
       m_own = m_new;
       float pr[C::kNIT];
       float psum = 0.f;
 #pragma unroll
       for (int it = 0; it < C::kNIT; ++it) {
-        pr[it] = exp2f(sc[it] - m_new);
+        pr[it] = ex2_approx(sc[it] - m_new);
         psum += pr[it];
       }
       l_own = l_own * a_own + psum;

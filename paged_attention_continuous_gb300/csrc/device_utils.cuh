@@ -156,6 +156,14 @@ __device__ __forceinline__ bool wait_counter_at_least(const uint32_t* counter, u
   }
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz.f32): relative error
+// about 2^-22, 2^-inf = +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void set_error(uint32_t* word, uint32_t bits) {
   if (word) atomicOr(word, bits);
 }

@@ -638,14 +638,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
       for (int it = 1; it < C::kNIT; ++it) pm = fmaxf(pm, sc[it]);
 #pragma unroll
       for (int o = C::kLG; o < 32; o <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
+      // the reference max moves only when a page raises it by more than 8
+      // (weights stay <= 2^8 in fp32), so the accumulators are rescaled
+      // rarely; a partial's (m, l, acc) share whatever reference it ends with
       const float m_new = fmaxf(m_own, pm);
-      const float a_own = ex2_approx(m_own - m_new);
-      m_own = m_new;
+      const float m_use = (m_new - m_own > 8.f) ? m_new : m_own;
+      const float a_own = (m_use == m_own) ? 1.f : ex2_approx(m_own - m_use);
+      m_own = m_use;
       float pr[C::kNIT];
       float psum = 0.f;
 #pragma unroll
       for (int it = 0; it < C::kNIT; ++it) {
-        pr[it] = ex2_approx(sc[it] - m_new);
+        pr[it] = ex2_approx(sc[it] - m_own);
         psum += pr[it];
       }
       l_own = l_own * a_own + psum;

@@ -47,7 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # decode kernel per workload (as ncu prints them: mixed 2048-token step 1.72
 # GB read + 10.32 MB written; 64-request decode step 566.31 MB + 8.71 MB);
 # cleared whenever the kernel changes.
-DECODE_TRAFFIC_BYTES = {"mixed_2048": 1.72e9 + 10.32e6, "decode_64": 566.31e6 + 8.71e6}
+DECODE_TRAFFIC_BYTES = {"mixed_2048": 1716275968 + 10705152, "decode_64": 566323456 + 8658432}
 
 
 def peaks():

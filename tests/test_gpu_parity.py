@@ -330,3 +330,33 @@ def test_workspace_reused_across_calls_of_different_sizes():
     torch.cuda.synchronize()
     assert ws.read_errors() == 0
     assert torch.equal(a, b)
+
+
+def test_trace_late_steps_sampled_all_layers():
+    """The request trace far past its start: every request runs on the GPU
+    (4 layers), while the oracle follows two long-lived requests that
+    arrive at steps 40 and 60 and, behind the queue, run from about step
+    460 and 720 to 930 and 1140 -- prefill through hundreds of decode steps
+    at sequence lengths up to ~1,900, on every layer."""
+    sc = workloads.trace_2000()
+    picks = []
+    for w in sc.waiting:
+        if w.arrival_step >= 40 + 20 * len(picks) and w.output_len >= 250 and w.prompt_len <= 3000:
+            picks.append(w.req_id)
+        if len(picks) == 2:
+            break
+    run = ParityRun(sc, sample=picks, arrivals=True)
+    seen_steps, longest = 0, 0
+    for step in range(1300):
+        st, g, r, toks = run.step()
+        assert st == 0
+        if len(toks):
+            for layer in range(sc.num_layers):
+                _check(g[layer], r[layer], "bf16", f"trace step {step} layer {layer}")
+            seen_steps += 1
+            rows = [i for i, rid in enumerate(run.last["req_ids"]) if int(rid) in picks]
+            longest = max([longest] + [int(run.last["seq_lens"][i]) for i in rows])
+        if all(p in run.o.requests and run.o.requests[p].state == "finished" for p in picks):
+            break
+    assert all(run.o.requests[p].state == "finished" for p in picks)
+    assert seen_steps > 600 and longest > 1500

@@ -70,3 +70,49 @@ def test_graph_replay_matches_eager_over_trace_steps():
     assert graph.workspace.read_errors() == 0
     assert ran > 30
     assert len(graph.graphs) < ran  # buckets are reused
+
+
+def test_graph_replay_matches_eager_sliding_window():
+    """The sliding-window trace (recycled pages, -1 entries in the tables):
+    graph replay of padded buckets equals the eager runner bit for bit."""
+    from paged_attention_continuous_gb300.step import GraphStepRunner, StepRunner
+    from tests.sched_driver import c_from_config, scenario_to_config
+    sc = workloads.sliding_trace(1)
+    s = c_from_config(scenario_to_config(sc))
+    kw = dict(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads, num_kv_heads=sc.num_kv_heads,
+              head_dim=sc.head_dim, dtype=sc.dtype, max_reqs=sc.max_requests_per_batch,
+              max_tokens=sc.max_batch_tokens, max_blocks_per_seq=sc.max_blocks_per_seq,
+              num_layers=sc.num_layers, device="cuda", sliding_window=sc.sliding_window)
+    eager, graph = StepRunner(**kw), GraphStepRunner(**kw)
+    nxt, ran, dropped = 0, 0, 0
+    for step in range(120):
+        while nxt < len(sc.waiting) and sc.waiting[nxt].arrival_step <= step:
+            w = sc.waiting[nxt]
+            s.add_request(w.req_id, w.prompt_len, w.output_len)
+            nxt += 1
+        st = s.schedule_step()
+        if st["status"] != 0 or st["num_reqs"] == 0:
+            if st["status"] == 0:
+                s.step_done()
+            continue
+        dropped += int((st["block_tables"][:, 0] < 0).sum())
+        T = st["num_tokens"]
+        ds = eager.upload(st)
+        key, _ = graph.prepare(st)
+        outs = []
+        for layer in range(sc.num_layers):
+            sd = [workloads.step_seed(sc.seed, step, layer, c) for c in range(3)]
+            q = workloads.token_tensors(T, sc.num_q_heads, sc.head_dim, seed=sd[0], device="cuda")
+            k = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=sd[1], device="cuda")
+            v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=sd[2], device="cuda")
+            outs.append(eager.run(ds, q, k, v, layer=layer))
+            graph.q_buf[layer][:T].copy_(q)
+            graph.k_buf[layer][:T].copy_(k)
+            graph.v_buf[layer][:T].copy_(v)
+        graph.run(key)
+        for layer in range(sc.num_layers):
+            assert torch.equal(graph.out_buf[layer][:T], outs[layer]), f"step {step} layer {layer}"
+        s.step_done()
+        ran += 1
+    assert eager.workspace.read_errors() == 0 and graph.workspace.read_errors() == 0
+    assert ran > 100 and dropped > 100

@@ -12,7 +12,12 @@
 // One CTA = (prefill row r, KV head g, a PAIR of 128-row query tiles).  A
 // query tile packs 128/G tokens x the G query heads that share KV head g, so
 // each K/V byte feeds G heads, and both tiles of the pair share every K/V
-// tile staged in shared memory.  Keys stream in tiles of 128 (eight 16-token
+// tile staged in shared memory.  The grid is flat over the pairs that exist,
+// times the KV heads (blockIdx.x = pair * Hkv + head; pairs counted row by
+// row, a row's latest -- heaviest -- pair first, so all heads of the
+// heaviest work launch first): warp 0 finds its CTA's row by a scan of the
+// rows' pair counts, so rows shorter than the longest chunk launch no idle
+// CTAs.  Keys stream in tiles of 128 (eight 16-token
 // pages), gathered through the block table by the TMA engine: one 2-D
 // tensor-map box of 16 rows x 64 dims per page half lands directly in the
 // 128-byte-swizzled canonical UMMA layout.
@@ -115,6 +120,7 @@ struct Params {
   const int32_t* seq_lens;
   const int32_t* block_tables;
   int32_t row_begin;          // first prefill row
+  int32_t num_rows;           // prefill rows
   int32_t num_tokens;         // rows of q / out
   int32_t num_blocks, max_blocks_per_seq, num_q_heads, num_kv_heads, group;
   float scale_log2;
@@ -172,17 +178,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int G = p.group;
   const int tpt = kBM / G;                       // tokens per query tile
-  const int r = p.row_begin + blockIdx.z;
-  const int g = blockIdx.y;
-  const int mp = gridDim.x - 1 - blockIdx.x;     // tile pair; heavy (late) pairs first
+  const int g = (int)(blockIdx.x % (unsigned)p.num_kv_heads);
+  // ---- which (row, pair) this CTA serves: warp 0 scans the rows' pair
+  // counts (ceil(q_len / pair tokens)); CTA (0, 0) also checks that no row
+  // has a negative query length or a zero one with context, and that the
+  // grid covers every pair
+  __shared__ int s_row, s_pair;
+  if (warp == 0) {
+    const int tpp = 2 * tpt;
+    const int x = (int)(blockIdx.x / (unsigned)p.num_kv_heads);
+    const int num_pairs = (int)(gridDim.x / (unsigned)p.num_kv_heads);
+    int run = 0, row = -1, pair = 0;
+    bool bad = false;
+    for (int b = 0; b < p.num_rows; b += 32) {
+      const int i = b + lane;
+      int cnt = 0;
+      if (i < p.num_rows) {
+        const int rr = p.row_begin + i;
+        const int ql = p.cu_seqlens_q[rr + 1] - p.cu_seqlens_q[rr];
+        if (ql < 0 || (ql == 0 && p.seq_lens[rr] != 0)) bad = true;
+        cnt = ql > 0 ? (ql + tpp - 1) / tpp : 0;
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const bool mine = cnt > 0 && x >= run + incl - cnt && x < run + incl;
+      const uint32_t hit = __ballot_sync(0xffffffffu, mine);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        row = __shfl_sync(0xffffffffu, i, src);
+        const int first = __shfl_sync(0xffffffffu, run + incl - cnt, src);
+        const int n = __shfl_sync(0xffffffffu, cnt, src);
+        pair = n - 1 - (x - first);              // the row's heaviest pair first
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    bad = __any_sync(0xffffffffu, bad) || run > num_pairs;
+    if (lane == 0) {
+      if (bad && blockIdx.x == 0) set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
+      s_row = row;
+      s_pair = pair;
+    }
+  }
+  __syncthreads();
+  if (s_row < 0) return;                         // past the last pair
+  const int r = p.row_begin + s_row;
+  const int mp = s_pair;
   const int q0 = p.cu_seqlens_q[r];
   const int q_len = p.cu_seqlens_q[r + 1] - q0;
   const int L = p.seq_lens[r];
   const int W = p.max_blocks_per_seq;
-  if (q_len == 0 && L == 0) return;  // a padding row
-  if (q_len < 1 || q0 < 0 || q0 + q_len > p.num_tokens || L < q_len || (L + kPage - 1) / kPage > W) {
-    if (threadIdx.x == 0 && blockIdx.x == gridDim.x - 1 && g == 0)
-      set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
+  if (q0 < 0 || q0 + q_len > p.num_tokens || L < q_len || (L + kPage - 1) / kPage > W) {
+    if (threadIdx.x == 0 && mp == 0 && g == 0) set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
     return;
   }
   const int tok0 = mp * 2 * tpt;                 // first token of query tile 0
@@ -601,6 +651,7 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   p.seq_lens = a.seq_lens;
   p.block_tables = a.block_tables;
   p.row_begin = a.num_decodes;
+  p.num_rows = a.num_reqs - a.num_decodes;
   p.num_tokens = a.num_tokens;
   p.num_blocks = a.num_blocks;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
@@ -611,7 +662,12 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   p.window = a.sliding_window;
   p.error_word = error_word;
   const int tpp = 2 * (kBM / G);  // tokens per CTA (a pair of query tiles)
-  dim3 grid((a.max_q_len + tpp - 1) / tpp, a.num_kv_heads, a.num_reqs - a.num_decodes);
+  // every row's pairs: at most (prefill tokens) / tpp rounded up per row
+  const int64_t pairs = ((int64_t)a.num_tokens - a.num_decodes + tpp - 1) / tpp +
+                        (a.num_reqs - a.num_decodes);
+  if (pairs <= 0) return CB_OK;
+  if (pairs * a.num_kv_heads >= ((int64_t)1 << 31)) return CB_ERR_UNSUPPORTED;
+  dim3 grid((unsigned)(pairs * a.num_kv_heads), 1, 1);
   prefill_kernel<<<grid, kThreads, smem, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(CB_ERR_CUDA, "prefill kernel launch: %s", cudaGetErrorString(e));

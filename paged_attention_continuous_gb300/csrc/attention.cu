@@ -253,8 +253,10 @@ extern "C" cb_status cb_paged_attention(const cb_attention_args* args, cb_stream
     // decode rows hold exactly one token each, so prefill tokens start at nd
     if (a.dtype == CB_DTYPE_BF16 && a.head_dim == 128 && cb::prefill_supported(G)) {
       uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+      // the decode kernel just queued (if any) reads and writes nothing the
+      // prefill rows use: let the prefill grid start on the SMs it frees
       st = cb::launch_prefill_bf16(a, reinterpret_cast<uint32_t*>(ws + L.header),
-                                   ws + L.prefill, stream);
+                                   ws + L.prefill, stream, nd > 0);
       if (st != CB_ERR_UNSUPPORTED) return st;
     }
     st = a.dtype == CB_DTYPE_BF16

@@ -217,6 +217,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const Params p) 
   __shared__ int32_t s_red2[kWarps];
   __shared__ int32_t s_spa, s_spb;
 
+  // a kernel launched after this one with programmatic serialization (the
+  // prefill rows of the same call, which read nothing this kernel writes)
+  // may start on SMs this grid has left
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nthreads = kWarps * 32;

@@ -623,7 +623,7 @@ bool prefill_supported(int group) {
 size_t prefill_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 
 cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, uint8_t*,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool overlap_previous) {
   using namespace prefill;
   if (a.head_dim != kD || a.block_size != kPage || a.dtype != CB_DTYPE_BF16) return CB_ERR_UNSUPPORTED;
   const int G = a.num_q_heads / a.num_kv_heads;
@@ -668,7 +668,18 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   if (pairs <= 0) return CB_OK;
   if (pairs * a.num_kv_heads >= ((int64_t)1 << 31)) return CB_ERR_UNSUPPORTED;
   dim3 grid((unsigned)(pairs * a.num_kv_heads), 1, 1);
-  prefill_kernel<<<grid, kThreads, smem, stream>>>(p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute lattr[1];
+  lattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  lattr[0].val.programmaticStreamSerializationAllowed = overlap_previous ? 1 : 0;
+  cfg.attrs = lattr;
+  cfg.numAttrs = 1;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, prefill_kernel, p);
+  if (le != cudaSuccess) return fail(CB_ERR_CUDA, "prefill kernel launch: %s", cudaGetErrorString(le));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(CB_ERR_CUDA, "prefill kernel launch: %s", cudaGetErrorString(e));
   return CB_OK;

@@ -19,7 +19,10 @@ size_t prefill_workspace_bytes(int64_t Hq, int64_t Hkv, int64_t D);
 
 // Launch the prefill-chunk kernel over rows [num_decodes, num_reqs) (bf16,
 // head_dim 128).  Returns CB_ERR_UNSUPPORTED if it cannot take this call.
+// overlap_previous: the kernel queued just before on `stream` is the decode
+// kernel of the same call; the prefill grid may start on the SMs it leaves
+// (programmatic stream serialization), as the two share no data.
 cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, uint8_t* scratch,
-                              cudaStream_t stream);
+                              cudaStream_t stream, bool overlap_previous);
 
 }  // namespace cb

@@ -213,6 +213,19 @@ def time_each(torch, fn, iters, stream):
     return sum(a.elapsed_time(b) for a, b in evs) / 1e3
 
 
+def time_median(torch, fn, iters, stream):
+    """Median per-launch device time (an event pair around every call)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(iters)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return float(np.median([a.elapsed_time(b) for a, b in evs])) / 1e3
+
+
 def time_loop(torch, fn, iters, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -295,7 +308,8 @@ def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
     """Long-prompt interleave: a 32,768-token prompt prefilled in 512-token
     chunks over 64 scheduler steps while 128 requests decode (64 Q / 8 KV
     heads, D = 128, budget 640).  Every step's append + attention is timed,
-    and its prefill and decode launches separately."""
+    and its prefill and decode launches separately (median of the reps of
+    each step)."""
     sc = workloads.long_prompt_32k()
     sched = load_c_scheduler(cb, sc)
     runner = _runner_for(sc, dev, torch)
@@ -323,9 +337,9 @@ def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
             fd()
         if fp:
             fp()
-        t_step = time_each(torch, full, reps, stream) / reps
-        t_dec = time_each(torch, fd, reps, stream) / reps if fd else 0.0
-        t_pre = time_each(torch, fp, reps, stream) / reps if fp else 0.0
+        t_step = time_median(torch, full, reps, stream)
+        t_dec = time_median(torch, fd, reps, stream) if fd else 0.0
+        t_pre = time_median(torch, fp, reps, stream) if fp else 0.0
         fl = prefill_flops(st, sc.num_q_heads, sc.head_dim)
         by = decode_bytes(st, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, 2)
         tot["tokens"] += T; tot["t_step"] += t_step; tot["t_pre"] += t_pre
@@ -542,7 +556,10 @@ def measure_swap(cb, torch, dev, reps=5):
     res = {}
     for name, f in (("swap_out", out), ("swap_in", back), ("memcpy_d2h", d2h), ("memcpy_h2d", h2d)):
         f()
-        t = time_each(torch, f, reps, stream) / reps
+        f()
+        # best of three rounds: a transfer over the CPU-GPU link can be
+        # slowed by other traffic on the host
+        t = min(time_each(torch, f, reps, stream) for _ in range(3)) / reps
         res[name + "_gbs"] = round(nbytes / t / 1e9, 1)
     torch.cuda.synchronize()
     assert int(ew.item()) == 0
@@ -838,7 +855,7 @@ def run_ours(args, rank, world):
     }
     if not args.no_extra and world == 1:
         line["decode_only"] = measure_decode_only(cb, torch, dev, max(K, 20), hbm)
-        line["long_prompt"] = measure_long_prompt(cb, torch, dev, 3, hbm, bf16, bf16s)
+        line["long_prompt"] = measure_long_prompt(cb, torch, dev, 5, hbm, bf16, bf16s)
         line["trace"] = measure_trace(cb, torch, dev, hbm, bf16)
         line["trace_graphs"] = measure_trace(cb, torch, dev, hbm, bf16, graphs=True)
         line["offload"] = {

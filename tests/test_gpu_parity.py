@@ -108,7 +108,8 @@ def test_decode_many_splits_and_rows():
                                             ("f32", 16, 4, 128)])
 def test_decode_few_long_rows(dtype, Hq, Hkv, D):
     """A handful of very long caches next to tiny ones: each long row is cut
-    into hundreds of splits (both phases), merged by the combine kernel."""
+    into hundreds of splits (both phases), merged in the same kernel by the
+    warps that run out of items."""
     sc = _decode_scenario([40001, 32768, 17, 2], Hq, Hkv, D, dtype)
     run = ParityRun(sc)
     st, g, r, _ = run.step()

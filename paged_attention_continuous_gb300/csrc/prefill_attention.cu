@@ -478,9 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_run = m_use;
       // p = 2^(s*scale - m) for a pair of scores at a time: one packed FMA,
       // the pair rounded to bf16, one packed bf16 ex2 -- which is already P
-      // in the bf16 layout the P.V MMA reads.  The row sum adds exactly those
-      // bf16 values in fp32 (4 packed chains).  P is written over the S
-      // columns (all read above).
+      // in the bf16 layout the P.V MMA reads.  The row sum adds those bf16
+      // values two pairs at a time in bf16 (one rounding, relative 2^-9),
+      // then in fp32 (4 packed chains).  P is written over the S columns
+      // (all read above).
       // a row with every key so far masked has m_use = -inf: subtract 0
       // instead, so its masked scores give 2^-inf = 0 rather than NaN
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
@@ -492,11 +493,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < 4; ++h) {
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
+        for (int i = 0; i < 32; i += 4) {
           const float2 x2 = __ffma2_rn(make_float2(sv[32 * h + i], sv[32 * h + i + 1]), sl2, nm2);
-          const uint32_t pb = fast_exp2_bf16x2(float2_to_bf16x2(x2.x, x2.y));
-          pk[i / 2] = pb;
-          ls2[(i >> 1) & 3] = __fadd2_rn(ls2[(i >> 1) & 3], bf16x2_to_float2(pb));
+          const float2 y2 = __ffma2_rn(make_float2(sv[32 * h + i + 2], sv[32 * h + i + 3]), sl2, nm2);
+          const uint32_t pa = fast_exp2_bf16x2(float2_to_bf16x2(x2.x, x2.y));
+          const uint32_t pb = fast_exp2_bf16x2(float2_to_bf16x2(y2.x, y2.y));
+          pk[i / 2] = pa;
+          pk[i / 2 + 1] = pb;
+          // two P pairs added in bf16 first (one rounding), then in fp32
+          uint32_t ps;
+          asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(ps) : "r"(pa), "r"(pb));
+          ls2[(i >> 2) & 3] = __fadd2_rn(ls2[(i >> 2) & 3], bf16x2_to_float2(ps));
         }
         tc::tmem_st16(trow + colS + 16 * h, pk);
       }

@@ -351,7 +351,10 @@ cb_status cb_kv_swap(const cb_swap_args* args, cb_stream_t stream);
  *   g = h / (Hq/Hkv).
  * Rows [0, num_decodes) must have query length 1 and run the split-KV decode
  * kernel (which also merges the splits of requests whose cache it split);
- * the remaining rows run the prefill-chunk kernel.  Both go to `stream`.
+ * the remaining rows run the prefill-chunk kernel.  Both go to `stream`;
+ * the prefill kernel may start on SMs the decode kernel has left (the two
+ * share no data), and work queued on `stream` after the call still runs
+ * after both.
  * With sliding_window = W > 0 the sum runs over j = p-W+1..p instead.
  * A row with query length 0 and seq_len 0 is padding and is skipped (no
  * error bit), so a step may be padded to a fixed shape (row counts, token

@@ -353,8 +353,8 @@ cb_status cb_kv_swap(const cb_swap_args* args, cb_stream_t stream);
  * kernel (which also merges the splits of requests whose cache it split);
  * the remaining rows run the prefill-chunk kernel.  Both go to `stream`;
  * the prefill kernel may start on SMs the decode kernel has left (the two
- * share no data), and work queued on `stream` after the call still runs
- * after both.
+ * share no data), and it completes only after the decode kernel, so work
+ * queued on `stream` after the call runs after both.
  * With sliding_window = W > 0 the sum runs over j = p-W+1..p instead.
  * A row with query length 0 and seq_len 0 is padding and is skipped (no
  * error bit), so a step may be padded to a fixed shape (row counts, token

@@ -167,6 +167,13 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// When this grid was launched to overlap the kernel before it (the decode
+// kernel of the same call), one thread of CTA 0 waits for that kernel before
+// exiting, on every path, so this grid completes only after it.
+__device__ __forceinline__ void order_after_previous_grid() {
+  if (blockIdx.x == 0 && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -224,7 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();
-  if (s_row < 0) return;                         // past the last pair
+  if (s_row < 0) {                               // past the last pair
+    order_after_previous_grid();
+    return;
+  }
   const int r = p.row_begin + s_row;
   const int mp = s_pair;
   const int q0 = p.cu_seqlens_q[r];
@@ -233,10 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int W = p.max_blocks_per_seq;
   if (q0 < 0 || q0 + q_len > p.num_tokens || L < q_len || (L + kPage - 1) / kPage > W) {
     if (threadIdx.x == 0 && mp == 0 && g == 0) set_error(p.error_word, CB_DEVERR_SEQ_RANGE);
+    order_after_previous_grid();
     return;
   }
   const int tok0 = mp * 2 * tpt;                 // first token of query tile 0
-  if (tok0 >= q_len) return;                     // this pair is past the chunk
+  if (tok0 >= q_len) {                           // this pair is past the chunk
+    order_after_previous_grid();
+    return;
+  }
   const bool has_t1 = tok0 + tpt < q_len;        // query tile 1 holds tokens
   const int start = L - q_len;
   const int last_tok = min(tok0 + 2 * tpt - 1, q_len - 1);
@@ -558,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
+  order_after_previous_grid();
 }
 
 // ------------------------------------------------------------------- host

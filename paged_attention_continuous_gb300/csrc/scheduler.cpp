@@ -287,8 +287,18 @@ void emit_step(cb_sched* s, int32_t num_decodes, cb_step* out) {
     max_q = std::max(max_q, n);
     max_seq = std::max(max_seq, s->seq_lens[i]);
     std::copy(r->blocks.begin(), r->blocks.end(), s->block_tables.begin() + (size_t)i * W);
-    for (int32_t pos = r->num_cached; pos < r->num_cached + n; ++pos)
-      s->slot_mapping.push_back(r->blocks[pos / bs] * bs + pos % bs);
+    // slot of position pos = blocks[pos / bs] * bs + pos % bs, walked block
+    // by block (one division per row, not per token)
+    int32_t pos = r->num_cached;
+    const int32_t end = r->num_cached + n;
+    while (pos < end) {
+      const int32_t bi = pos / bs;
+      const int32_t off = pos - bi * bs;
+      const int32_t run = std::min(bs - off, end - pos);
+      const int32_t base = r->blocks[bi] * bs + off;
+      for (int32_t k = 0; k < run; ++k) s->slot_mapping.push_back(base + k);
+      pos += run;
+    }
   }
   out->num_reqs = R;
   out->num_tokens = s->cu_seqlens_q[R];
@@ -491,6 +501,21 @@ cb_status cb_sched_create(const cb_config* cfg, cb_sched** out) {
   s->cfg.initial_free_list = nullptr;
   s->reserved_blocks = (int64_t)std::ceil((double)cfg->safety_margin * (double)cfg->num_blocks);
   for (int32_t i = 0; i < cfg->swap_blocks; ++i) s->swap_free.push_back(i);
+  // touch the per-step output arrays once (up to 16 MB) so that the first
+  // scheduled step does not pay their page faults
+  {
+    const size_t rows = (size_t)cfg->max_requests_per_batch;
+    const size_t table = rows * (size_t)cfg->max_blocks_per_seq;
+    if (table * sizeof(int32_t) <= ((size_t)16 << 20)) {
+      s->block_tables.assign(table, -1);
+      s->block_tables.clear();
+    }
+    s->slot_mapping.assign((size_t)cfg->max_batch_tokens, 0);
+    s->slot_mapping.clear();
+    s->req_ids.assign(rows, 0);
+    s->cu_seqlens_q.assign(rows + 1, 0);
+    s->seq_lens.assign(rows, 0);
+  }
   s->refs.assign(cfg->num_blocks, 0);
   s->init_pos.resize(cfg->num_blocks);
   s->in_init.assign(cfg->num_blocks, 0);

@@ -293,6 +293,30 @@ cb_status cb_sched_swapped(const cb_sched* s, int64_t* out, int32_t capacity,
                            int32_t* count, int32_t* free_slots);
 
 /* ------------------------------------------------------------------------
+ * cb_validate_step (host).  Checks a step's metadata, given as HOST arrays,
+ * against what cb_kv_append and cb_paged_attention require, and names the
+ * first row or token that breaks a rule (CB_ERR_INVALID_ARG, message in
+ * cb_last_error()):
+ *   - cu_seqlens_q[0] >= 0 and non-decreasing, cu_seqlens_q[num_reqs] <=
+ *     num_tokens; rows [0, num_decodes) have one query (or are padding);
+ *   - a row with no queries has seq_len 0 (padding); otherwise seq_len >=
+ *     its query length and ceil(seq_len / block_size) <= max_blocks_per_seq;
+ *   - every block id the row's queries read (from the first query's window
+ *     with sliding_window > 0) lies in [0, num_blocks);
+ *   - slot_mapping (optional, may be NULL) entries lie in [-1, num_blocks *
+ *     block_size).
+ * With CB_VALIDATE=1 in the environment, cb_paged_attention and
+ * cb_kv_append copy their metadata back (synchronising the stream) and run
+ * these checks before launching, except while the stream is being captured
+ * into a CUDA graph.
+ * ---------------------------------------------------------------------- */
+cb_status cb_validate_step(const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                           const int32_t* block_tables, const int32_t* slot_mapping,
+                           int32_t num_reqs, int32_t num_decodes, int32_t num_tokens,
+                           int32_t max_blocks_per_seq, int32_t num_blocks,
+                           int32_t block_size, int32_t sliding_window);
+
+/* ------------------------------------------------------------------------
  * cb_kv_append (GPU).  "vLLM serving internals", PagedAttention as a virtual
  * memory system: token t's K/V goes to block slot_mapping[t] / block_size,
  * offset slot_mapping[t] % block_size, for every KV head.

@@ -134,6 +134,7 @@ def _declare():
     L.cb_sched_swapped.argtypes = [vp, P(ctypes.c_int64), i32, P(i32), P(i32)]
     L.cb_kv_append.argtypes = [vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, vp, vp]
     L.cb_kv_swap.argtypes = [P(cb_swap_args), vp]
+    L.cb_validate_step.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32]
     L.cb_attention_workspace_size.argtypes = [i32, i32, i32, i32]
     L.cb_attention_workspace_size.restype = sz
     L.cb_attention_workspace_init.argtypes = [vp, sz, vp]
@@ -143,6 +144,7 @@ def _declare():
                  "cb_sched_prefix_stats", "cb_add_running_request",
                  "cb_schedule_step", "cb_step_done", "cb_request_slots", "cb_sched_counts",
                  "cb_sched_free_list", "cb_sched_swapped", "cb_kv_append", "cb_kv_swap",
+                 "cb_validate_step",
                  "cb_attention_workspace_init",
                  "cb_paged_attention", "cb_attention_read_errors"):
         getattr(L, name).restype = ctypes.c_int
@@ -374,6 +376,24 @@ def kv_swap(src_pools, dst_pools, src_ids, dst_ids, *, error_word=None, stream=N
     _check(_lib.cb_kv_swap(ctypes.byref(a), _stream_ptr(stream)))
 
 
+def validate_step(step: dict, *, num_blocks: int, block_size: int = 16,
+                  sliding_window: int = 0) -> None:
+    """cb_validate_step on a scheduler step's host arrays (numpy); raises
+    CBError naming the first broken rule."""
+    R = int(step["num_reqs"])
+    keep = [np.ascontiguousarray(np.asarray(step[k], dtype=np.int32).reshape(-1))
+            for k in ("cu_seqlens_q", "seq_lens", "block_tables")]
+    bt = np.asarray(step["block_tables"]).reshape(R, -1) if R else np.zeros((0, 1))
+    W = int(bt.shape[1]) if R else int(step.get("max_blocks_per_seq", 1) or 1)
+    sm = step.get("slot_mapping")
+    sm = None if sm is None else np.ascontiguousarray(np.asarray(sm, dtype=np.int32))
+    T = int(step["num_tokens"])
+    _check(_lib.cb_validate_step(keep[0].ctypes.data, keep[1].ctypes.data, keep[2].ctypes.data,
+                                 None if sm is None else sm.ctypes.data, R,
+                                 int(step["num_decodes"]), T, W, int(num_blocks),
+                                 int(block_size), int(sliding_window)))
+
+
 def workspace_size(num_reqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
     return int(_lib.cb_attention_workspace_size(num_reqs, num_q_heads, num_kv_heads, head_dim))
 
@@ -433,5 +453,5 @@ def paged_attention_args(**kw) -> cb_attention_args:
     return cb_attention_args(**kw)
 
 
-__all__ = ["Scheduler", "kv_append", "kv_swap", "paged_attention", "Workspace", "workspace_size",
+__all__ = ["Scheduler", "kv_append", "kv_swap", "validate_step", "paged_attention", "Workspace", "workspace_size",
            "CBError", "version", "library", "LIB_PATH"]

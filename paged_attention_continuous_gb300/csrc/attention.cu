@@ -13,6 +13,7 @@
 #include "device_utils.cuh"
 #include "prefill_dispatch.h"
 #include "simt_attention.cuh"
+#include "validate.h"
 
 namespace cb {
 
@@ -236,6 +237,10 @@ extern "C" cb_status cb_paged_attention(const cb_attention_args* args, cb_stream
   if (a.workspace_bytes < L.total)
     return fail(CB_ERR_INVALID_ARG, "workspace too small: %zu < %zu", a.workspace_bytes, L.total);
 
+  if (cb::validate_enabled()) {
+    cb_status vs = cb::validate_attention_call(a, stream);
+    if (vs != CB_OK) return vs;
+  }
   const int nd = a.num_decodes;
   const int G = a.num_q_heads / a.num_kv_heads;
   cb_status st = CB_OK;

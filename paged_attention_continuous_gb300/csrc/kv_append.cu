@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include "cb_error.h"
+#include "validate.h"
 #include "device_utils.cuh"
 
 namespace cb {
@@ -67,6 +68,11 @@ extern "C" cb_status cb_kv_append(const void* k_new, const void* v_new,
     return cb::fail(CB_ERR_UNSUPPORTED, "cb_kv_append: head_dim*elem must be a multiple of 16");
   const uintptr_t align = (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_cache | (uintptr_t)v_cache;
   if (align & 15u) return cb::fail(CB_ERR_INVALID_ARG, "cb_kv_append: pointers must be 16-byte aligned");
+  if (cb::validate_enabled()) {
+    cb_status vs = cb::validate_append_call(slot_mapping, num_tokens, num_blocks, block_size,
+                                            (cudaStream_t)stream);
+    if (vs != CB_OK) return vs;
+  }
   int shift = 0;
   while ((1 << shift) < block_size) ++shift;
   const int vecs = row_bytes / 16;

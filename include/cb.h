@@ -281,6 +281,17 @@ cb_status cb_sched_counts(const cb_sched* s, int32_t* free_blocks,
 cb_status cb_sched_free_list(const cb_sched* s, int32_t* out, int32_t capacity,
                              int32_t* count);
 
+/* Fault injection (a test hook for memory pressure; between steps only,
+ * CB_ERR_STATE while a step is open).  cb_sched_hold_blocks takes up to n
+ * blocks out of the allocatable pool exactly as allocation would (free
+ * queue head first, then the newest initialized blocks, demoted), writes
+ * their ids to out_ids and their number to *count; they stay out until
+ * cb_sched_release_blocks puts them back at the free queue's tail, in the
+ * given order (CB_ERR_INVALID_ARG, nothing released, if an id is not held
+ * or is listed twice). */
+cb_status cb_sched_hold_blocks(cb_sched* s, int32_t n, int32_t* out_ids, int32_t* count);
+cb_status cb_sched_release_blocks(cb_sched* s, const int32_t* ids, int32_t n);
+
 /* Prefix caching counters (any pointer may be NULL): prompt tokens reused
  * from cached blocks so far, keyed blocks, keyed blocks in the initialized
  * pool (free but still matchable). */

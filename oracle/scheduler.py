@@ -127,6 +127,12 @@ Readings where the pages leave a step open:
    blocks at the same table positions).  Prefix caching is refused with a
    window (sliding layers do not share blocks).
 
+14. Fault injection (not on the pages; a test hook for memory pressure):
+   hold_blocks(n) takes up to n blocks out of the allocatable pool exactly
+   as allocation would (free queue head first, then the newest
+   initialized blocks, demoted), between steps; release_blocks(ids) puts
+   them back at the free queue's tail in the given order.
+
 Parity: pinned by hand-derived traces (tests/golden/scheduler_*.json) and by
 invariants (budget, cap, FIFO order, block conservation, all-or-nothing
 admission); the full batch composition beyond the pages' rules rests on the
@@ -205,6 +211,7 @@ class FifoScheduler:
         self.block_key: Dict[int, tuple] = {}
         self.free_init: List[int] = []
         self.prefix_hit_tokens = 0
+        self.held: List[int] = []   # blocks taken out by hold_blocks
         self.waiting: collections.deque = collections.deque()
         self.running: List[Request] = []
         self.requests: Dict[int, Request] = {}
@@ -270,6 +277,32 @@ class FifoScheduler:
                 break
             out.append(b)
         return out
+
+    # ------------------------------------------------- fault injection
+    def hold_blocks(self, n: int) -> List[int]:
+        """Take up to n blocks out of the allocatable pool, as allocation
+        would (free queue head, then the newest initialized blocks), to
+        simulate memory taken by something else; they stay out until
+        release_blocks."""
+        if self._pending is not None:
+            raise RuntimeError("a step is open")
+        out = []
+        while len(out) < n and self._num_free() > 0:
+            out.append(self._alloc())
+        self.held.extend(out)
+        return out
+
+    def release_blocks(self, ids) -> None:
+        """Return held blocks to the free queue's tail, in the given order."""
+        if self._pending is not None:
+            raise RuntimeError("a step is open")
+        ids = [int(b) for b in ids]
+        if len(set(ids)) != len(ids) or any(b not in self.held for b in ids):
+            raise ValueError("not a held block")
+        for b in ids:
+            self.held.remove(b)
+            del self.refs[b]
+            self.free.append(b)
 
     def free_list(self) -> List[int]:
         """Allocatable blocks: the free queue, then the initialized pool."""

@@ -125,6 +125,8 @@ def _declare():
     L.cb_add_request.argtypes = [vp, i64, i32, i32]
     L.cb_add_request_tokens.argtypes = [vp, i64, i32, i32, P(i32), i32]
     L.cb_sched_prefix_stats.argtypes = [vp, P(i64), P(i32), P(i32)]
+    L.cb_sched_hold_blocks.argtypes = [vp, i32, P(i32), P(i32)]
+    L.cb_sched_release_blocks.argtypes = [vp, P(i32), i32]
     L.cb_add_running_request.argtypes = [vp, i64, i32, i32, i32]
     L.cb_schedule_step.argtypes = [vp, P(cb_step)]
     L.cb_step_done.argtypes = [vp, P(i32), P(P(i64))]
@@ -141,7 +143,8 @@ def _declare():
     L.cb_paged_attention.argtypes = [P(cb_attention_args), vp]
     L.cb_attention_read_errors.argtypes = [vp, sz, vp, P(ctypes.c_uint32)]
     for name in ("cb_sched_create", "cb_add_request", "cb_add_request_tokens",
-                 "cb_sched_prefix_stats", "cb_add_running_request",
+                 "cb_sched_prefix_stats", "cb_sched_hold_blocks", "cb_sched_release_blocks",
+                 "cb_add_running_request",
                  "cb_schedule_step", "cb_step_done", "cb_request_slots", "cb_sched_counts",
                  "cb_sched_free_list", "cb_sched_swapped", "cb_kv_append", "cb_kv_swap",
                  "cb_validate_step",
@@ -220,6 +223,22 @@ class Scheduler:
         _check(_lib.cb_add_request_tokens(self._h, req_id, prompt_len, output_len,
                                           t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
                                           int(t.shape[0])))
+
+    def hold_blocks(self, n: int) -> list:
+        """Fault injection: take up to n blocks out of the allocatable pool
+        (``cb_sched_hold_blocks``); returns their ids."""
+        out = np.zeros(max(int(n), 1), dtype=np.int32)
+        k = ctypes.c_int32()
+        _check(_lib.cb_sched_hold_blocks(self._h, int(n),
+                                         out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                         ctypes.byref(k)))
+        return out[:k.value].tolist()
+
+    def release_blocks(self, ids) -> None:
+        """Return held blocks to the free queue's tail, in order."""
+        a = np.ascontiguousarray(np.asarray(list(ids), dtype=np.int32))
+        _check(_lib.cb_sched_release_blocks(self._h, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                            int(a.shape[0])))
 
     def prefix_stats(self):
         """(prompt tokens reused so far, keyed blocks, keyed blocks in the

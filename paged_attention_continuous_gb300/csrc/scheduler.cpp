@@ -184,6 +184,7 @@ struct cb_sched {
   std::vector<int32_t> block_tokens;               // its own tokens [num_blocks][bs]
   std::unordered_map<cb::Fp, int32_t, cb::FpHash> index;
   int64_t prefix_hits = 0;
+  std::vector<char> held;                          // taken by cb_sched_hold_blocks
 };
 
 namespace {
@@ -517,6 +518,7 @@ cb_status cb_sched_create(const cb_config* cfg, cb_sched** out) {
     s->seq_lens.assign(rows, 0);
   }
   s->refs.assign(cfg->num_blocks, 0);
+  s->held.assign(cfg->num_blocks, 0);
   s->init_pos.resize(cfg->num_blocks);
   s->in_init.assign(cfg->num_blocks, 0);
   s->keyed.assign(cfg->num_blocks, 0);
@@ -810,6 +812,38 @@ cb_status cb_sched_free_list(const cb_sched* s, int32_t* out, int32_t capacity, 
       if (i >= capacity) break;
       out[i++] = b;
     }
+  }
+  return CB_OK;
+}
+
+cb_status cb_sched_hold_blocks(cb_sched* s, int32_t n, int32_t* out_ids, int32_t* count) {
+  if (!s || n < 0 || (n > 0 && !out_ids)) return cb::fail(CB_ERR_INVALID_ARG, "bad argument");
+  if (s->step_open) return cb::fail(CB_ERR_STATE, "a step is open; call cb_step_done first");
+  int32_t k = 0;
+  while (k < n && num_free(s) > 0) {
+    const int32_t b = alloc_block(s);
+    s->held[b] = 1;
+    out_ids[k++] = b;
+  }
+  if (count) *count = k;
+  return CB_OK;
+}
+
+cb_status cb_sched_release_blocks(cb_sched* s, const int32_t* ids, int32_t n) {
+  if (!s || n < 0 || (n > 0 && !ids)) return cb::fail(CB_ERR_INVALID_ARG, "bad argument");
+  if (s->step_open) return cb::fail(CB_ERR_STATE, "a step is open; call cb_step_done first");
+  std::vector<char> seen(s->held.size(), 0);
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t b = ids[i];
+    if (b < 0 || b >= (int32_t)s->held.size() || !s->held[b] || seen[b])
+      return cb::fail(CB_ERR_INVALID_ARG, "block %d is not held (or listed twice)", b);
+    seen[b] = 1;
+  }
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t b = ids[i];
+    s->held[b] = 0;
+    s->refs[b] = 0;
+    s->free_list.push_back(b);
   }
   return CB_OK;
 }

@@ -15,12 +15,21 @@
  *   4. cb_step_done      (host)  commits the step: advances each request,
  *      finishes requests and returns their blocks to the pool.
  *
+ * Around the step: cb_kv_swap (GPU) moves offloaded requests' blocks to and
+ * from a pinned host swap pool; cb_validate_step (host) checks a step's
+ * metadata; cb_paged_decode_noalloc runs decode rows without a caller
+ * workspace; the scheduler options cover the PrefillFirst policy, prefill
+ * caps, offloading with soft reset, prefix caching with eviction
+ * (cb_add_request_tokens) and sliding-window layers, and
+ * cb_sched_hold_blocks / cb_sched_release_blocks inject memory pressure.
+ *
  * Sources (page title, section):
  *   - "Continuous batching architecture" (HF Transformers docs): Request
  *     lifecycle; Chunked prefill; Scheduler (token budget max_batch_tokens,
  *     cache budget, request cap max_requests_per_batch); FIFO; Admission
  *     (all-or-nothing, safety_margin); Offloading (stalled requests and their
- *     block demand).
+ *     block demand; offloading to a CPU swap pool; Soft reset); Prefix
+ *     caching; Eviction; PrefillFirst; Memory management (sliding layers).
  *   - "Chunked Prefill" (Ultralytics glossary): How chunked prefill works
  *     (decode tokens first, then chunks; each chunk attends under a causal
  *     mask over absolute positions to all earlier chunks plus itself).

@@ -160,7 +160,7 @@ class StepRunner:
         if R > self.max_reqs or T > self.max_tokens:
             raise ValueError("step larger than the runner was sized for")
         W = self.W
-        bt = np.asarray(step["block_tables"], dtype=np.int32).reshape(R, -1)
+        bt = np.asarray(step["block_tables"], dtype=np.int32).reshape(R, -1 if R else W)
         if bt.shape[1] != W:
             raise ValueError("block_tables width differs from max_blocks_per_seq")
         o1 = R + 1
@@ -384,7 +384,7 @@ class GraphStepRunner:
         if Tb > self.T_cap or Rb > self.R_cap:
             raise ValueError("step larger than the runner was sized for")
         W = self.W
-        bt = np.asarray(step["block_tables"], dtype=np.int32).reshape(R, -1)
+        bt = np.asarray(step["block_tables"], dtype=np.int32).reshape(R, -1 if R else W)
         if bt.shape[1] != W:
             raise ValueError("block_tables width differs from max_blocks_per_seq")
         b = self._turn

@@ -1,0 +1,63 @@
+"""Host-side pieces of the step runners, on the CPU.
+
+StepRunner._pack lays a step's metadata out as one int32 run (cu_seqlens_q,
+seq_lens, block_tables, slot_mapping) for a single pinned copy; every
+runner's device views are slices of it at the returned offsets.  bucket()
+gives the padding intervals of the graph runner.
+"""
+import numpy as np
+import pytest
+
+from paged_attention_continuous_gb300.step import StepRunner, bucket
+
+
+def _host_runner(max_reqs, max_tokens, W):
+    # the packing needs no device state: build the object without __init__
+    r = object.__new__(StepRunner)
+    r.max_reqs, r.max_tokens, r.W = max_reqs, max_tokens, W
+    return r
+
+
+def _step():
+    return {"num_reqs": 3, "num_decodes": 2, "num_tokens": 6,
+            "cu_seqlens_q": np.array([0, 1, 2, 6], dtype=np.int32),
+            "seq_lens": np.array([17, 5, 40], dtype=np.int32),
+            "block_tables": np.array([[7, 8, -1], [9, -1, -1], [1, 2, 3]], dtype=np.int32),
+            "slot_mapping": np.array([128, 148, 36, 37, 38, 39], dtype=np.int32)}
+
+
+def test_pack_layout():
+    r = _host_runner(4, 8, 3)
+    st = _step()
+    h = np.full(64, -7, dtype=np.int32)
+    n, (o1, o2, o3) = r._pack(st, h)
+    assert (o1, o2, o3, n) == (4, 7, 16, 22)
+    assert list(h[:o1]) == [0, 1, 2, 6]
+    assert list(h[o1:o2]) == [17, 5, 40]
+    assert list(h[o2:o3]) == [7, 8, -1, 9, -1, -1, 1, 2, 3]
+    assert list(h[o3:n]) == [128, 148, 36, 37, 38, 39]
+    assert h[n] == -7                       # nothing written past the run
+
+
+def test_pack_refuses_oversized_or_misshapen_steps():
+    st = _step()
+    with pytest.raises(ValueError):
+        _host_runner(2, 8, 3)._pack(st, np.zeros(64, np.int32))     # 3 rows > 2
+    with pytest.raises(ValueError):
+        _host_runner(4, 5, 3)._pack(st, np.zeros(64, np.int32))     # 6 tokens > 5
+    with pytest.raises(ValueError):
+        _host_runner(4, 8, 4)._pack(st, np.zeros(64, np.int32))     # table width 3 != 4
+
+
+def test_empty_step_packs_to_one_word():
+    r = _host_runner(4, 8, 3)
+    st = {"num_reqs": 0, "num_decodes": 0, "num_tokens": 0,
+          "cu_seqlens_q": np.zeros(1, np.int32), "seq_lens": np.zeros(0, np.int32),
+          "block_tables": np.zeros((0, 3), np.int32), "slot_mapping": np.zeros(0, np.int32)}
+    n, _ = r._pack(st, np.zeros(8, np.int32))
+    assert n == 1
+
+
+def test_bucket_intervals():
+    assert [bucket(n) for n in (0, 1, 2, 3, 5, 64, 65, 1000)] == [0, 1, 2, 4, 8, 64, 128, 1024]
+    assert [bucket(n, 16) for n in (0, 1, 16, 17)] == [0, 16, 16, 32]

@@ -61,3 +61,56 @@ def test_empty_step_packs_to_one_word():
 def test_bucket_intervals():
     assert [bucket(n) for n in (0, 1, 2, 3, 5, 64, 65, 1000)] == [0, 1, 2, 4, 8, 64, 128, 1024]
     assert [bucket(n, 16) for n in (0, 1, 16, 17)] == [0, 16, 16, 32]
+
+
+class _Ev:
+    def record(self, *a):
+        pass
+
+    def synchronize(self):
+        pass
+
+
+class _Cuda:
+    Event = _Ev
+
+
+class _TorchStub:
+    cuda = _Cuda
+
+
+def test_graph_runner_pads_to_buckets():
+    """3 decodes and 3 prefill rows (chunks 2, 3, 1): buckets (16 tokens,
+    4 decode rows, 4 prefill rows, chunk 4); rows are real decodes, one
+    decode padding row, real prefills, one prefill padding row; padding rows
+    have no queries, seq_len 0 and -1 tables; padding tokens slot -1."""
+    import torch
+    from paged_attention_continuous_gb300.step import GraphStepRunner
+    g = object.__new__(GraphStepRunner)
+    g.torch = _TorchStub
+    g.swap = None
+    g.W, g.T_cap, g.R_cap = 3, 64, 16
+    cap = 1024
+    g._host = [torch.zeros(cap, dtype=torch.int32) for _ in range(2)]
+    g._copied = [None, None]
+    g._turn = 0
+    g._dev = torch.zeros(cap, dtype=torch.int32)
+    st = {"num_reqs": 6, "num_decodes": 3, "num_tokens": 9,
+          "cu_seqlens_q": np.array([0, 1, 2, 3, 5, 8, 9], dtype=np.int32),
+          "seq_lens": np.array([10, 20, 30, 2, 40, 7], dtype=np.int32),
+          "block_tables": np.array([[1, -1, -1], [2, 3, -1], [4, 5, 6], [7, -1, -1],
+                                    [8, 9, 10], [11, -1, -1]], dtype=np.int32),
+          "slot_mapping": np.arange(100, 109, dtype=np.int32)}
+    key, T = g.prepare(st)
+    assert key == (16, 4, 4, 4) and T == 9
+    d = g._dev.numpy()
+    Rb, W = 8, 3
+    cu = d[0:Rb + 1]
+    sl = d[Rb + 1:2 * Rb + 1]
+    bt = d[2 * Rb + 1:2 * Rb + 1 + Rb * W].reshape(Rb, W)
+    sm = d[2 * Rb + 1 + Rb * W:2 * Rb + 1 + Rb * W + 16]
+    assert list(cu) == [0, 1, 2, 3, 3, 5, 8, 9, 9]
+    assert list(sl) == [10, 20, 30, 0, 2, 40, 7, 0]
+    assert bt[3].tolist() == [-1, -1, -1] and bt[7].tolist() == [-1, -1, -1]
+    assert bt[1].tolist() == [2, 3, -1] and bt[5].tolist() == [8, 9, 10]
+    assert list(sm[:9]) == list(range(100, 109)) and (sm[9:] == -1).all()

@@ -114,3 +114,45 @@ def test_graph_runner_pads_to_buckets():
     assert bt[3].tolist() == [-1, -1, -1] and bt[7].tolist() == [-1, -1, -1]
     assert bt[1].tolist() == [2, 3, -1] and bt[5].tolist() == [8, 9, 10]
     assert list(sm[:9]) == list(range(100, 109)) and (sm[9:] == -1).all()
+
+
+def test_swap_pool_orders_swap_ins_before_swap_outs(monkeypatch):
+    """SwapPool.apply queues every swap-in (slot -> block) before any
+    swap-out (block -> slot), each over every layer's K and V, chunked to
+    at most 128 pools per call; the ids it passes are the step's pairs."""
+    import torch
+    import paged_attention_continuous_gb300.step as step_mod
+    calls = []
+
+    def fake_kv_swap(src, dst, src_ids, dst_ids, error_word=None):
+        calls.append((list(src), list(dst), src_ids.tolist(), dst_ids.tolist()))
+
+    monkeypatch.setattr(step_mod, "kv_swap", fake_kv_swap)
+    p = object.__new__(step_mod.SwapPool)
+    p.torch = _TorchStub
+    layers = 70                                    # 140 pools: two calls per direction
+    cache = [("cache", i) for i in range(2 * layers)]
+    pool = [("pool", i) for i in range(2 * layers)]
+    p._cache, p._pool = cache, pool
+    p.swap_blocks = 8
+    p.block_bytes = 4096
+    p._host = [torch.zeros(32, dtype=torch.int32) for _ in range(2)]
+    p._copied = [None, None]
+    p._turn = 0
+    p._dev = torch.zeros(32, dtype=torch.int32)
+    p.error_word = None
+    step = {"swap_in": np.array([[3, 10], [5, 11]], dtype=np.int32),      # (slot, block)
+            "swap_out": np.array([[20, 3], [21, 6], [22, 7]], dtype=np.int32)}  # (block, slot)
+    moved = p.apply(step)
+    assert moved == 5 * 2 * layers * 4096
+    assert [len(c[0]) for c in calls] == [128, 12, 128, 12]
+    for c in calls[:2]:                            # swap-ins: pool -> cache
+        assert c[0][0][0] == "pool" and c[1][0][0] == "cache"
+        assert c[2] == [3, 5] and c[3] == [10, 11]
+    for c in calls[2:]:                            # swap-outs: cache -> pool
+        assert c[0][0][0] == "cache" and c[1][0][0] == "pool"
+        assert c[2] == [20, 21, 22] and c[3] == [3, 6, 7]
+    assert calls[0][0][0] == ("pool", 0) and calls[1][0][0] == ("pool", 128)
+    calls.clear()
+    assert p.apply({"swap_in": np.zeros((0, 2)), "swap_out": np.zeros((0, 2))}) == 0
+    assert not calls

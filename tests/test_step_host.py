@@ -156,3 +156,91 @@ def test_swap_pool_orders_swap_ins_before_swap_outs(monkeypatch):
     calls.clear()
     assert p.apply({"swap_in": np.zeros((0, 2)), "swap_out": np.zeros((0, 2))}) == 0
     assert not calls
+
+
+def test_pipelined_runner_dependencies(monkeypatch):
+    """PipelinedStepRunner.submit, with recording stand-ins for streams and
+    events: step n uses buffer set n % 2; its copy-in waits for the compute
+    of step n-2 (same set), its compute waits for its own copy-in and for
+    the copy-out of step n-2 (the set's output buffer), and its copy-out
+    waits for its compute."""
+    import contextlib
+    import torch
+    from paged_attention_continuous_gb300.step import PipelinedStepRunner
+    log = []
+
+    class Ev:
+        n = 0
+
+        def __init__(self):
+            Ev.n += 1
+            self.id = Ev.n
+            self.tag = None
+
+        def record(self, stream=None):
+            self.tag = (stream.name, len(log))
+            log.append(("record", stream.name, self.id))
+
+        def synchronize(self):
+            pass
+
+    class Stream:
+        def __init__(self, name):
+            self.name = name
+
+        def wait_event(self, ev):
+            log.append(("wait", self.name, ev.id))
+
+    current = {"s": None}
+
+    @contextlib.contextmanager
+    def stream_ctx(s):
+        prev, current["s"] = current["s"], s
+        yield
+        current["s"] = prev
+
+    class Cuda:
+        Event = Ev
+        stream = staticmethod(stream_ctx)
+
+    class TorchStub:
+        cuda = Cuda
+
+    r = object.__new__(PipelinedStepRunner)
+    r.torch = TorchStub
+    r.swap = None
+    r.max_reqs, r.max_tokens, r.W = 4, 8, 3
+    r.k_cache = [None]
+    L = 1
+    mk = lambda: [torch.zeros(8, 2, 4) for _ in range(L)]
+    r._sets = [dict(q=mk(), k=mk(), v=mk(), out=mk(), meta=torch.zeros(64, dtype=torch.int32),
+                    stage=torch.zeros(64, dtype=torch.int32)) for _ in range(2)]
+    r.in_stream, r.compute_stream, r.out_stream = Stream("in"), Stream("compute"), Stream("out")
+    r._copied_in, r._computed, r._copied_out = [None, None], [None, None], [None, None]
+    r._slot = 0
+    runs = []
+    r.run = lambda ds, q, k, v, layer=0, out=None: runs.append(current["s"].name)
+    step = _step()
+    events = []
+    for n in range(4):
+        before = len(log)
+        ev = r.submit(step, torch.zeros(6, 2, 4), torch.zeros(6, 2, 4), torch.zeros(6, 2, 4),
+                      torch.zeros(6, 2, 4))
+        events.append([e for e in log[before:]])
+    assert runs == ["compute"] * 4
+    # event ids per step: copy_in, computed, copied_out are created in order
+    ids = []
+    for n, evs in enumerate(events):
+        rec = [e for e in evs if e[0] == "record"]
+        assert [e[1] for e in rec] == ["in", "compute", "out"]
+        ids.append({"in": rec[0][2], "comp": rec[1][2], "out": rec[2][2]})
+    for n, evs in enumerate(events):
+        waits = [(e[1], e[2]) for e in evs if e[0] == "wait"]
+        want = []
+        if n >= 2:
+            want.append(("in", ids[n - 2]["comp"]))
+        want.append(("compute", ids[n]["in"]))
+        if n >= 2:
+            want.append(("compute", ids[n - 2]["out"]))
+        want.append(("out", ids[n]["comp"]))
+        assert waits == want, (n, waits, want)

@@ -468,6 +468,27 @@ cb_status cb_attention_read_errors(void* workspace, size_t workspace_bytes,
                                    cb_stream_t stream, uint32_t* bits);
 
 /* ------------------------------------------------------------------------
+ * cb_debug_inject_wait_timeout (test hook; no counterpart in the pages).
+ *
+ * Every device wait of the attention kernels is bounded: a wait that runs
+ * out records CB_DEVERR_TIMEOUT, the kernel drains what it started and
+ * returns, and the workspace is left ready for the next call (the failure
+ * detection of "Continuous batching architecture" carried to the device,
+ * without a GPU fault).  This hook lets a test make such a wait run out:
+ *   wait_ns       limit of every bounded wait of later launches (0: the
+ *                 default of 1 s);
+ *   decode_item   >= 0: the decode kernel announces the first page of its
+ *                 work item with this index but never copies it;
+ *   prefill_tile  >= 0: CTA 0 of the prefill kernel announces its K tile
+ *                 with this index but never copies it;
+ *                 -1 for either: nothing is withheld.
+ * The call itself launches nothing; it affects launches made after it,
+ * from any thread.  Not for production use.
+ * ---------------------------------------------------------------------- */
+cb_status cb_debug_inject_wait_timeout(uint64_t wait_ns, int32_t decode_item,
+                                       int32_t prefill_tile);
+
+/* ------------------------------------------------------------------------
  * cb_paged_decode_noalloc (GPU).  No counterpart in the pages: an extra
  * entry point for callers that cannot allocate device memory.
  *

@@ -142,6 +142,7 @@ def _declare():
     L.cb_attention_workspace_init.argtypes = [vp, sz, vp]
     L.cb_paged_attention.argtypes = [P(cb_attention_args), vp]
     L.cb_attention_read_errors.argtypes = [vp, sz, vp, P(ctypes.c_uint32)]
+    L.cb_debug_inject_wait_timeout.argtypes = [ctypes.c_uint64, i32, i32]
     for name in ("cb_sched_create", "cb_add_request", "cb_add_request_tokens",
                  "cb_sched_prefix_stats", "cb_sched_hold_blocks", "cb_sched_release_blocks",
                  "cb_add_running_request",
@@ -149,7 +150,8 @@ def _declare():
                  "cb_sched_free_list", "cb_sched_swapped", "cb_kv_append", "cb_kv_swap",
                  "cb_validate_step",
                  "cb_attention_workspace_init",
-                 "cb_paged_attention", "cb_attention_read_errors"):
+                 "cb_paged_attention", "cb_attention_read_errors",
+                 "cb_debug_inject_wait_timeout"):
         getattr(L, name).restype = ctypes.c_int
 
 
@@ -464,6 +466,13 @@ def paged_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens, block_tables, *
                           workspace.nbytes, int(sliding_window))
     _check(_lib.cb_paged_attention(ctypes.byref(a), _stream_ptr(stream)))
     return out
+
+
+def inject_wait_timeout(wait_ns: int = 0, decode_item: int = -1, prefill_tile: int = -1) -> None:
+    """cb_debug_inject_wait_timeout (test hook): shorten every bounded device
+    wait of later launches to ``wait_ns`` (0 restores 1 s) and withhold the
+    copies of one decode work item / one prefill K tile (-1: none)."""
+    _check(_lib.cb_debug_inject_wait_timeout(int(wait_ns), int(decode_item), int(prefill_tile)))
 
 
 def paged_attention_args(**kw) -> cb_attention_args:

@@ -6,11 +6,10 @@
 // row-generic CUDA-core kernel.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "cb_error.h"
-#include "decode_attention.cuh"
+#include "decode_launch.h"
 #include "device_utils.cuh"
+#include "launch_common.h"
 #include "prefill_dispatch.h"
 #include "simt_attention.cuh"
 #include "validate.h"
@@ -27,23 +26,24 @@ struct WsLayout {
   int64_t slots = 0;  // decode partial slots
 };
 
-// Workspace regions.  The header, the decode split counters and the prefill
+// Workspace regions.  The header, the decode split tickets and the prefill
 // region hold state that must read zero at the start of every call (each
 // call leaves them zero), so they sit at FIXED offsets that do not depend on
 // the call's sizes.  The split partials are scratch rewritten by every call,
 // sized by the call's decode rows.
-//   header words: [0] device error bits, [1] decode item counter,
-//                 [2] prefill item counter, [3] decode merge counter
-//   counters: done[kPlanMax * kMaxKvHeads], merged[kPlanMax * kMaxKvHeads]
+//   header words: [0] device error bits, [1] decode item counter
+//   counters: done[kPlanMax * kMaxKvHeads] (one ticket counter per
+//             (decode row, KV head) of a launch)
 constexpr int64_t kMaxKvHeads = 64;
-constexpr size_t kCounterWords = (size_t)decode::kPlanMax * kMaxKvHeads;
+constexpr int kPlanMax = decode::kPlanMax;
+constexpr size_t kCounterWords = (size_t)kPlanMax * kMaxKvHeads;
 
 WsLayout ws_layout(int64_t num_reqs, int64_t Hq, int64_t Hkv, int64_t D) {
   WsLayout w;
-  const int64_t rows = num_reqs < decode::kPlanMax ? num_reqs : decode::kPlanMax;
+  const int64_t rows = num_reqs < kPlanMax ? num_reqs : kPlanMax;
   w.header = 0;
   w.counters = kAlign;
-  w.prefill = w.counters + align_up(2 * kCounterWords * 4);
+  w.prefill = w.counters + align_up(kCounterWords * 4);
   w.part_ml = w.prefill + align_up(prefill_workspace_bytes(Hq, Hkv, D));
   const size_t slots = (size_t)decode::partial_slots(rows, Hkv);
   w.part_acc = w.part_ml + align_up(slots * Hq * 2 * 4);
@@ -52,84 +52,15 @@ WsLayout ws_layout(int64_t num_reqs, int64_t Hq, int64_t Hkv, int64_t D) {
   return w;
 }
 
-int sm_count() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 152;
-  });
-  return n;
-}
-
-template <typename T, int D, int G>
-constexpr int decode_warps() {
-  using WS = decode::WarpSmem<T, D, G, 2>;
-  return sizeof(WS) * 8 + decode::kPlanSmemBytes <= 200 * 1024 ? 8 : 4;
-}
-
-template <typename T, int D, int G, bool kWindow>
-cb_status launch_decode(const cb_attention_args& a, const WsLayout& L, cudaStream_t stream) {
-  constexpr int kStages = 2;
-  constexpr int kWarps = decode_warps<T, D, G>();
-  using WS = decode::WarpSmem<T, D, G, kStages>;
-  const size_t smem = sizeof(WS) * kWarps + decode::kPlanSmemBytes;
-  auto kern = decode::decode_kernel<T, D, G, kWarps, kStages, kWindow>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [&] {
-    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  });
-  if (attr_err != cudaSuccess)
-    return fail(CB_ERR_CUDA, "decode kernel smem attribute: %s", cudaGetErrorString(attr_err));
+decode::Scratch decode_scratch(const cb_attention_args& a, const WsLayout& L) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  decode::Params p{};
-  p.q = a.q;
-  p.out = a.out;
-  p.k_cache = a.k_cache;
-  p.v_cache = a.v_cache;
-  p.cu_seqlens_q = a.cu_seqlens_q;
-  p.seq_lens = a.seq_lens;
-  p.block_tables = a.block_tables;
-  p.num_tokens = a.num_tokens;
-  p.num_blocks = a.num_blocks;
-  p.max_blocks_per_seq = a.max_blocks_per_seq;
-  p.num_q_heads = a.num_q_heads;
-  p.num_kv_heads = a.num_kv_heads;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.window = a.sliding_window;
-  p.error_word = reinterpret_cast<uint32_t*>(ws + L.header);
-  p.work_counter = reinterpret_cast<uint32_t*>(ws + L.header) + 1;
-  p.merge_counter = reinterpret_cast<uint32_t*>(ws + L.header) + 3;
-  p.done = reinterpret_cast<uint32_t*>(ws + L.counters);
-  p.merged = p.done + kCounterWords;
-  p.max_slots = (int32_t)(L.slots < (1 << 30) ? L.slots : (1 << 30));
-  p.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
-  p.part_acc = reinterpret_cast<float*>(ws + L.part_acc);
-  const int grid = sm_count();
-  for (int r0 = 0; r0 < a.num_decodes; r0 += decode::kPlanMax) {
-    p.row_begin = r0;
-    p.num_rows = a.num_decodes - r0 < decode::kPlanMax ? a.num_decodes - r0 : decode::kPlanMax;
-    kern<<<grid, kWarps * 32, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(CB_ERR_CUDA, "decode kernel launch: %s", cudaGetErrorString(e));
-  }
-  return CB_OK;
-}
-
-template <typename T>
-cb_status dispatch_decode(const cb_attention_args& a, const WsLayout& L, cudaStream_t s) {
-  const int G = a.num_q_heads / a.num_kv_heads;
-#define CB_DEC(DD, GG)                                                               \
-  if (a.head_dim == DD && G == GG)                                                   \
-    return a.sliding_window > 0 ? launch_decode<T, DD, GG, true>(a, L, s)            \
-                                : launch_decode<T, DD, GG, false>(a, L, s);
-  CB_DEC(128, 1) CB_DEC(128, 2) CB_DEC(128, 4) CB_DEC(128, 8)
-  CB_DEC(64, 1) CB_DEC(64, 2) CB_DEC(64, 4) CB_DEC(64, 8)
-#undef CB_DEC
-  return CB_ERR_UNSUPPORTED;
+  decode::Scratch s{};
+  s.work_counter = reinterpret_cast<uint32_t*>(ws + L.header) + 1;
+  s.done = reinterpret_cast<uint32_t*>(ws + L.counters);
+  s.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
+  s.part_acc = reinterpret_cast<float*>(ws + L.part_acc);
+  s.slots = L.slots;
+  return s;
 }
 
 template <typename T, int D>
@@ -245,8 +176,10 @@ extern "C" cb_status cb_paged_attention(const cb_attention_args* args, cb_stream
   const int G = a.num_q_heads / a.num_kv_heads;
   cb_status st = CB_OK;
   if (nd > 0) {
-    st = a.dtype == CB_DTYPE_BF16 ? cb::dispatch_decode<__nv_bfloat16>(a, L, stream)
-                                  : cb::dispatch_decode<float>(a, L, stream);
+    const cb::decode::Scratch ds = cb::decode_scratch(a, L);
+    uint32_t* ew = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) + L.header);
+    st = a.dtype == CB_DTYPE_BF16 ? cb::decode::dispatch_bf16(a, ds, ew, stream)
+                                  : cb::decode::dispatch_f32(a, ds, ew, stream);
     if (st == CB_ERR_UNSUPPORTED) {
       st = a.dtype == CB_DTYPE_BF16
                ? cb::dispatch_simt<__nv_bfloat16>(a, L, 0, nd, 0, nd, stream)

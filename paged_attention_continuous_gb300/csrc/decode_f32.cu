@@ -1,0 +1,24 @@
+// Split-KV decode kernel instantiations for fp32 caches (CUDA-core path):
+// head_dim 64 and 128, 1 to 8 query heads per KV head, with and without a
+// sliding window.
+#include "decode_launch.cuh"
+
+namespace cb {
+namespace decode {
+
+cb_status dispatch_f32(const cb_attention_args& a, const Scratch& s, uint32_t* error_word,
+                       cudaStream_t stream) {
+  using T = float;
+  const int G = a.num_q_heads / a.num_kv_heads;
+#define CB_DEC(DD, GG)                                                              \
+  if (a.head_dim == DD && G == GG)                                                  \
+    return a.sliding_window > 0 ? launch<T, DD, GG, true>(a, s, error_word, stream) \
+                                : launch<T, DD, GG, false>(a, s, error_word, stream);
+  CB_DEC(128, 1) CB_DEC(128, 2) CB_DEC(128, 4) CB_DEC(128, 8)
+  CB_DEC(64, 1) CB_DEC(64, 2) CB_DEC(64, 4) CB_DEC(64, 8)
+#undef CB_DEC
+  return CB_ERR_UNSUPPORTED;
+}
+
+}  // namespace decode
+}  // namespace cb

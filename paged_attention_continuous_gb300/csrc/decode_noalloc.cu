@@ -21,13 +21,13 @@
 #include <mutex>
 
 #include "cb_error.h"
-#include "decode_attention.cuh"
+#include "decode_launch.h"
+#include "launch_common.h"
 
 namespace cb {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = CB_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_decode_scratch[kNoAllocScratchBytes];
 
@@ -40,12 +40,12 @@ size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 // As many partial slots as the decode plan would like, or as fit in the
 // array; at least 2 per row are needed (the plan then uses larger splits).
+// Hq, Hkv and D are validated (positive) before this is called.
 NoAllocLayout noalloc_layout(int64_t rows, int64_t Hq, int64_t Hkv, int64_t D) {
   NoAllocLayout l;
-  // [0, 256): word 1 item counter, word 3 merge counter; then done[rows *
-  // Hkv] and merged[rows * Hkv]
+  // [0, 256): word 1 item counter; then the split tickets done[rows * Hkv]
   l.counters = 256;
-  l.part_ml = l.counters + up256((size_t)rows * Hkv * 2 * 4);
+  l.part_ml = l.counters + up256((size_t)rows * Hkv * 4);
   const size_t per_slot = (size_t)Hq * (D + 2) * 4;
   const size_t room = kNoAllocScratchBytes - l.part_ml - 512;  // two roundings to 256
   int64_t slots = decode::partial_slots(rows, Hkv);
@@ -60,81 +60,22 @@ NoAllocLayout noalloc_layout(int64_t rows, int64_t Hq, int64_t Hkv, int64_t D) {
 std::mutex g_mu;
 uint8_t* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up once).
+// Device address of the scratch array on the current device (set up once
+// per device, with that device current).
 cb_status scratch_for_current_device(uint8_t** out) {
   int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(CB_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return fail(CB_ERR_UNSUPPORTED, "device index %d", dev);
+  cb_status st = current_device(&dev);
+  if (st != CB_OK) return st;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_scratch_ptr[dev]) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess || !p)
       return fail(CB_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
     g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
   }
   *out = g_scratch_ptr[dev];
   return CB_OK;
-}
-
-template <typename T, int D, int G, bool kWindow>
-cb_status launch(const cb_attention_args& a, uint8_t* scratch, const NoAllocLayout& L,
-                 uint32_t* error_word, cudaStream_t stream) {
-  constexpr int kStages = 2;
-  using WS8 = decode::WarpSmem<T, D, G, kStages>;
-  constexpr int kWarps = sizeof(WS8) * 8 + decode::kPlanSmemBytes <= 200 * 1024 ? 8 : 4;
-  const size_t smem = sizeof(WS8) * kWarps + decode::kPlanSmemBytes;
-  auto kern = decode::decode_kernel<T, D, G, kWarps, kStages, kWindow>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return fail(CB_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  decode::Params p{};
-  p.q = a.q;
-  p.out = a.out;
-  p.k_cache = a.k_cache;
-  p.v_cache = a.v_cache;
-  p.cu_seqlens_q = a.cu_seqlens_q;
-  p.seq_lens = a.seq_lens;
-  p.block_tables = a.block_tables;
-  p.row_begin = 0;
-  p.num_rows = a.num_decodes;
-  p.num_tokens = a.num_tokens;
-  p.num_blocks = a.num_blocks;
-  p.max_blocks_per_seq = a.max_blocks_per_seq;
-  p.num_q_heads = a.num_q_heads;
-  p.num_kv_heads = a.num_kv_heads;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.window = a.sliding_window;
-  p.error_word = error_word;
-  p.work_counter = reinterpret_cast<uint32_t*>(scratch) + 1;
-  p.merge_counter = reinterpret_cast<uint32_t*>(scratch) + 3;
-  p.done = reinterpret_cast<uint32_t*>(scratch + L.counters);
-  p.merged = p.done + (size_t)a.num_decodes * a.num_kv_heads;
-  p.max_slots = (int32_t)L.slots;
-  p.part_ml = reinterpret_cast<float*>(scratch + L.part_ml);
-  p.part_acc = reinterpret_cast<float*>(scratch + L.part_acc);
-  kern<<<sms > 0 ? sms : 152, kWarps * 32, smem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(CB_ERR_CUDA, "decode kernel launch: %s", cudaGetErrorString(e));
-  return CB_OK;
-}
-
-template <typename T>
-cb_status dispatch(const cb_attention_args& a, uint8_t* s, const NoAllocLayout& L, uint32_t* ew,
-                   cudaStream_t st) {
-  const int G = a.num_q_heads / a.num_kv_heads;
-#define CB_NA(DD, GG)                                                   \
-  if (a.head_dim == DD && G == GG)                                      \
-    return a.sliding_window > 0 ? launch<T, DD, GG, true>(a, s, L, ew, st) \
-                                : launch<T, DD, GG, false>(a, s, L, ew, st);
-  CB_NA(128, 1) CB_NA(128, 2) CB_NA(128, 4) CB_NA(128, 8)
-  CB_NA(64, 1) CB_NA(64, 2) CB_NA(64, 4) CB_NA(64, 8)
-#undef CB_NA
-  return fail(CB_ERR_UNSUPPORTED, "no-alloc decode: head_dim %d with %d query heads per KV head",
-              a.head_dim, G);
 }
 
 }  // namespace
@@ -154,6 +95,13 @@ extern "C" cb_status cb_paged_decode_noalloc(const cb_attention_args* args, uint
     return fail(CB_ERR_INVALID_ARG, "NULL pointer argument");
   if (a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.num_q_heads % a.num_kv_heads != 0)
     return fail(CB_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  if (a.num_kv_heads > 64) return fail(CB_ERR_UNSUPPORTED, "num_kv_heads > 64");
+  if (a.head_dim != 64 && a.head_dim != 128)
+    return fail(CB_ERR_UNSUPPORTED, "no-alloc decode: head_dim must be 64 or 128");
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const int max_g = a.dtype == CB_DTYPE_BF16 ? 16 : 8;
+  if (G > max_g || (G & (G - 1)) != 0)
+    return fail(CB_ERR_UNSUPPORTED, "no-alloc decode: %d query heads per KV head", G);
   if (a.block_size != 16) return fail(CB_ERR_UNSUPPORTED, "block_size must be 16");
   if (a.dtype != CB_DTYPE_F32 && a.dtype != CB_DTYPE_BF16) return fail(CB_ERR_INVALID_ARG, "unknown dtype");
   if (a.num_blocks <= 0 || a.max_blocks_per_seq <= 0) return fail(CB_ERR_INVALID_ARG, "bad pool sizes");
@@ -178,6 +126,16 @@ extern "C" cb_status cb_paged_decode_noalloc(const cb_attention_args* args, uint
   // zero when the kernel starts
   cudaError_t e = cudaMemsetAsync(scratch, 0, L.zeroed, stream);
   if (e != cudaSuccess) return fail(CB_ERR_CUDA, "clearing scratch: %s", cudaGetErrorString(e));
-  return a.dtype == CB_DTYPE_BF16 ? cb::dispatch<__nv_bfloat16>(a, scratch, L, error_word, stream)
-                                  : cb::dispatch<float>(a, scratch, L, error_word, stream);
+  cb::decode::Scratch ds{};
+  ds.work_counter = reinterpret_cast<uint32_t*>(scratch) + 1;
+  ds.done = reinterpret_cast<uint32_t*>(scratch + L.counters);
+  ds.part_ml = reinterpret_cast<float*>(scratch + L.part_ml);
+  ds.part_acc = reinterpret_cast<float*>(scratch + L.part_acc);
+  ds.slots = L.slots;
+  st = a.dtype == CB_DTYPE_BF16 ? cb::decode::dispatch_bf16(a, ds, error_word, stream)
+                                : cb::decode::dispatch_f32(a, ds, error_word, stream);
+  if (st == CB_ERR_UNSUPPORTED)
+    return fail(CB_ERR_UNSUPPORTED, "no-alloc decode: head_dim %d with %d query heads per KV head",
+                a.head_dim, G);
+  return st;
 }

@@ -72,15 +72,17 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once
+// limit_ns nanoseconds have passed without it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -137,23 +139,6 @@ __device__ __forceinline__ void lane0_fetch_add1(uint32_t* counter, uint32_t& va
       : "+r"(value)
       : "l"(counter), "r"(lane)
       : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Wait until *counter >= target (acquire); false after kWaitTimeoutNs.
-__device__ __forceinline__ bool wait_counter_at_least(const uint32_t* counter, uint32_t target) {
-  if (ld_acquire_gpu(counter) >= target) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    __nanosleep(100);
-    if (ld_acquire_gpu(counter) >= target) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
-  }
 }
 
 // 2^x with the hardware approximation (ex2.approx.ftz.f32): relative error

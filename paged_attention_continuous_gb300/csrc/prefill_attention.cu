@@ -61,13 +61,14 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include <cstring>
-#include <mutex>
+#include <atomic>
 
 #include "cb_error.h"
 #include "device_utils.cuh"
+#include "launch_common.h"
 #include "prefill_dispatch.h"
 #include "tcgen05.cuh"
+#include "tensor_map.h"
 
 namespace cb {
 namespace prefill {
@@ -126,6 +127,9 @@ struct Params {
   float scale_log2;
   int32_t window;             // sliding window (0: full attention)
   uint32_t* error_word;
+  uint64_t wait_ns;           // limit of every bounded wait
+  int32_t withhold_tile;      // test hook: CTA 0 never copies its K tile with
+                              // this ring index (-1: none)
 };
 
 __device__ __forceinline__ void abort_cta(Bars* B, uint32_t* error_word) {
@@ -133,8 +137,8 @@ __device__ __forceinline__ void abort_cta(Bars* B, uint32_t* error_word) {
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Bars* B,
-                                              uint32_t* error_word) {
-  if (mbar_wait(bar, parity)) return true;
+                                              uint32_t* error_word, uint64_t limit_ns) {
+  if (mbar_wait(bar, parity, limit_ns)) return true;
   abort_cta(B, error_word);
   return false;
 }
@@ -327,15 +331,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* full = hv ? &B->v_full[s] : &B->k_full[s];
       if (jj >= nst) {
         uint64_t* empty = hv ? &B->v_empty[s] : &B->k_empty[s];
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(empty, ((jj / nst) - 1) & 1));
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(empty, ((jj / nst) - 1) & 1, p.wait_ns));
         if (!ok) { abort_cta(B, p.error_word); break; }
       }
       if (*reinterpret_cast<volatile uint32_t*>(&B->abort)) break;
       if (lane == 0) mbar_arrive_expect_tx(full, kTileBytes);
+      // test hook: the withheld tile is announced but never copied, so the
+      // bounded waits on it run out
+      const bool withhold = hv == 0 && blockIdx.x == 0 && jj == p.withhold_tile;
 #pragma unroll
       for (int pg = 0; pg < kBN / kPage; ++pg) {
         const int rr = __shfl_sync(0xffffffffu, row, pg);
-        if (lane == 0) {
+        if (lane == 0 && !withhold) {
           uint8_t* d = smem + ring + s * kTileBytes + pg * (kPage * 128);
           tc::tma_load_2d(d, tmap, 0, rr, full);
           tc::tma_load_2d(d + kHalf, tmap, 64, rr, full);
@@ -346,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // drain: every issued copy lands before the CTA may exit
     for (int j = (issued > nst ? issued - nst : 0); j < issued; ++j)
-      mbar_wait(hv ? &B->v_full[j % nst] : &B->k_full[j % nst], (j / nst) & 1);
+      mbar_wait(hv ? &B->v_full[j % nst] : &B->k_full[j % nst], (j / nst) & 1, p.wait_ns);
   } else if (warp >= kMmaWarp) {
     // ------------------------------------------------------------------ MMA
     // Warp kMmaWarp + t issues the MMAs of query tile t: per KV tile j,
@@ -374,8 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int jr = jj - 1;            // ring position of the previous tile
           const int jp = j_lo + jr;         // its KV tile
           const int sp = jr % kStagesV;
-          ok = wait_or_abort(&B->p_full[t], jr & 1, B, p.error_word) &&
-               wait_or_abort(&B->v_full[sp], (jr / kStagesV) & 1, B, p.error_word);
+          ok = wait_or_abort(&B->p_full[t], jr & 1, B, p.error_word, p.wait_ns) &&
+               wait_or_abort(&B->v_full[sp], (jr / kStagesV) & 1, B, p.error_word, p.wait_ns);
           if (!ok) break;
           if ((L & (kPage - 1)) != 0 && jp == (L - 1) / kBN) {
             // rows L .. end of the last page hold pool slots past the
@@ -402,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (jj < nt) {
           const int s = jj % kStagesK;
-          ok = wait_or_abort(&B->k_full[s], (jj / kStagesK) & 1, B, p.error_word);
+          ok = wait_or_abort(&B->k_full[s], (jj / kStagesK) & 1, B, p.error_word, p.wait_ns);
           if (!ok) break;
           const uint64_t bk = dk0 + s * kTileDesc;
 #pragma unroll
@@ -416,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // drain: all issued MMAs complete before tensor memory is released
       tc::mma_commit(&B->drain[t]);
-      mbar_wait(&B->drain[t], 0);
+      mbar_wait(&B->drain[t], 0, p.wait_ns);
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -453,11 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile j, softmax 0 of tile j + 1, ...), so each runs alone on the
       // SM's exp and FMA units while the tensor core works for the other
       if (has_t1 && (t == 1 || jj >= 1)) {
-        const bool tw = __all_sync(0xffffffffu, t == 0 ? mbar_wait(&B->p_full[1], (jj - 1) & 1)
-                                                     : mbar_wait(&B->p_full[0], jj & 1));
+        const bool tw = __all_sync(0xffffffffu, t == 0 ? mbar_wait(&B->p_full[1], (jj - 1) & 1, p.wait_ns)
+                                                     : mbar_wait(&B->p_full[0], jj & 1, p.wait_ns));
         if (!tw) { abort_cta(B, p.error_word); ok = false; break; }
       }
-      bool w = __all_sync(0xffffffffu, mbar_wait(&B->s_full[t], jj & 1));
+      bool w = __all_sync(0xffffffffu, mbar_wait(&B->s_full[t], jj & 1, p.wait_ns));
       if (!w) { abort_cta(B, p.error_word); ok = false; break; }
       tc::fence_after_sync();
       const int kbase = (j_lo + jj) * kBN;
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // epilogue: O_t / l -> bf16 rows
     if (ok) {
-      const bool w = __all_sync(0xffffffffu, mbar_wait(&B->o_done[t], 0));
+      const bool w = __all_sync(0xffffffffu, mbar_wait(&B->o_done[t], 0, p.wait_ns));
       if (!w) abort_cta(B, p.error_word);
       if (w) {
         tc::fence_after_sync();
@@ -575,67 +582,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   order_after_previous_grid();
 }
 
-// ------------------------------------------------------------------- host
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// 2-D view of a cache as [num_blocks * Hkv * 16 rows][128 dims] bf16; box 16
-// rows x 64 dims (128 bytes) with the 128-byte swizzle; rows past the end
-// read as zeros.
-cb_status make_cache_map(CUtensorMap* m, const void* base, int64_t rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
-  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kPage};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(CB_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return CB_OK;
-}
-// Tensor maps depend only on the cache's base address and size, so the last
-// few are kept (a step calls the kernel once per layer, K and V each).
-cb_status cached_cache_map(CUtensorMap* m, const void* base, int64_t rows) {
-  struct Entry {
-    const void* base;
-    int64_t rows;
-    CUtensorMap map;
-  };
-  constexpr int kEntries = 64;
-  static Entry entries[kEntries];
-  static int used = 0, next = 0;
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < used; ++i)
-    if (entries[i].base == base && entries[i].rows == rows) {
-      *m = entries[i].map;
-      return CB_OK;
-    }
-  cb_status st = make_cache_map(m, base, rows);
-  if (st != CB_OK) return st;
-  entries[next] = Entry{base, rows, *m};
-  next = (next + 1) % kEntries;
-  if (used < kEntries) ++used;
-  return CB_OK;
-}
 }  // namespace prefill
 
 bool prefill_supported(int group) {
@@ -651,19 +597,15 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   const int G = a.num_q_heads / a.num_kv_heads;
   if (!prefill_supported(G)) return CB_ERR_UNSUPPORTED;
   const size_t smem = SmemLayout::total + 1024;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [&] {
-    attr = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem);
-  });
-  if (attr != cudaSuccess) return fail(CB_ERR_CUDA, "prefill smem attribute: %s", cudaGetErrorString(attr));
+  static std::atomic<uint8_t> attr_set[kMaxDevices];
+  cb_status st = ensure_smem_attr(reinterpret_cast<const void*>(prefill_kernel), smem, attr_set);
+  if (st != CB_OK) return st;
   const int64_t rows = (int64_t)a.num_blocks * a.num_kv_heads * kPage;
   if (rows >= ((int64_t)1 << 31) - kPage) return CB_ERR_UNSUPPORTED;
   Params p{};
-  cb_status st = cached_cache_map(&p.tmap_k, a.k_cache, rows);
+  st = cached_cache_map(&p.tmap_k, a.k_cache, rows, kD);
   if (st != CB_OK) return st;
-  st = cached_cache_map(&p.tmap_v, a.v_cache, rows);
+  st = cached_cache_map(&p.tmap_v, a.v_cache, rows, kD);
   if (st != CB_OK) return st;
   p.k_cache = a.k_cache;
   p.v_cache = a.v_cache;
@@ -683,6 +625,8 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.window = a.sliding_window;
   p.error_word = error_word;
+  p.wait_ns = wait_limit_ns();
+  p.withhold_tile = withheld_prefill_tile();
   const int tpp = 2 * (kBM / G);  // tokens per CTA (a pair of query tiles)
   // every row's pairs: at most (prefill tokens) / tpp rounded up per row
   const int64_t pairs = ((int64_t)a.num_tokens - a.num_decodes + tpp - 1) / tpp +

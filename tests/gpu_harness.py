@@ -32,14 +32,25 @@ def tolerance_ok(gpu: np.ndarray, ref: np.ndarray, dtype: str):
     return bool((err <= bound).all()), float(err.max(initial=0.0)), float((err - bound).max(initial=-1))
 
 
+RUNNERS = ("eager", "graph", "pipelined")
+
+
 class ParityRun:
     """``arrivals``: add each waiting request before the step numbered by its
-    arrival_step (a trace), instead of all of them up front."""
+    arrival_step (a trace), instead of all of them up front.
+
+    ``runner`` picks the CUDA step path compared with the oracle: "eager"
+    (StepRunner: upload + append + attention on the current stream),
+    "graph" (GraphStepRunner: the step padded to its bucket and replayed
+    from a CUDA graph) or "pipelined" (PipelinedStepRunner: inputs and
+    output in pinned host memory, copied on their own streams)."""
 
     def __init__(self, sc, sample=None, device="cuda", fill_seed=1234, max_tokens=None,
-                 arrivals=False):
-        import paged_attention_continuous_gb300 as cb
-        from paged_attention_continuous_gb300.step import StepRunner
+                 arrivals=False, runner="eager"):
+        from paged_attention_continuous_gb300.step import (GraphStepRunner,
+                                                           PipelinedStepRunner, StepRunner)
+        assert runner in RUNNERS, runner
+        self.kind = runner
         self.sc = sc
         self.dtype = sc.dtype
         cfg = scenario_to_config(sc)
@@ -54,7 +65,9 @@ class ParityRun:
         else:
             load_scenario(self.o, sc)
             load_scenario(self.c, sc)
-        self.runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
+        Runner = {"eager": StepRunner, "graph": GraphStepRunner,
+                  "pipelined": PipelinedStepRunner}[runner]
+        self.runner = Runner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
                                  num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim,
                                  dtype=sc.dtype, max_reqs=sc.max_requests_per_batch,
                                  max_tokens=max_tokens or sc.max_batch_tokens,
@@ -62,6 +75,7 @@ class ParityRun:
                                  num_layers=sc.num_layers, device=device,
                                  swap_blocks=sc.swap_blocks, sliding_window=sc.sliding_window)
         self.device = device
+        self.torch = torch
         self.pristine = []
         for layer in range(sc.num_layers):
             kp = workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size, sc.head_dim,
@@ -121,9 +135,45 @@ class ParityRun:
                 for layer in range(self.sc.num_layers)]
         self.swap_pairs += len(st["swap_in"]) + len(st["swap_out"])
 
-    def step(self):
+    def _gpu_step(self, sg, qkv):
+        """Run one scheduled step through the chosen CUDA path; qkv[layer] =
+        (q, k, v) on the device.  Returns the outputs per layer (device or
+        pinned host tensors with the step's T rows)."""
+        r = self.runner
+        T = int(sg["num_tokens"])
+        if self.kind == "eager":
+            ds = r.upload(sg)
+            return [r.run(ds, q, k, v, layer=layer) for layer, (q, k, v) in enumerate(qkv)]
+        if self.kind == "graph":
+            key, _ = r.prepare(sg)
+            for layer, (q, k, v) in enumerate(qkv):
+                r.q_buf[layer][:T].copy_(q)
+                r.k_buf[layer][:T].copy_(k)
+                r.v_buf[layer][:T].copy_(v)
+            r.run(key)
+            return [r.out_buf[layer][:T] for layer in range(len(qkv))]
+        # pipelined: the step's inputs and output live in pinned host memory
+        hq = [q.cpu().pin_memory() for q, _, _ in qkv]
+        hk = [k.cpu().pin_memory() for _, k, _ in qkv]
+        hv = [v.cpu().pin_memory() for _, _, v in qkv]
+        ho = [self.torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for q, _, _ in qkv]
+        r.submit(sg, hq, hk, hv, ho).synchronize()
+        return ho
+
+    def _gpu_no_batch(self, sg):
+        """A step that found no batch may still carry swaps: queue them where
+        the chosen runner queues its kernels."""
+        if self.kind == "pipelined":
+            with self.torch.cuda.stream(self.runner.compute_stream):
+                self.runner.apply_swaps(sg)
+            return
+        self.runner.apply_swaps(sg)
+
+    def step(self, check=True):
         """One step on both sides.  Returns (status, gpu_out[layer] as float64
-        numpy for followed rows, oracle_out[layer], followed token indices)."""
+        numpy for followed rows, oracle_out[layer], followed token indices).
+        With check=False the oracle appends the followed rows' K/V but skips
+        attention (and nothing is compared): (status, None, None, toks)."""
         sc = self.sc
         if self.arrivals:
             while (self.next_arrival < len(sc.waiting) and
@@ -138,7 +188,7 @@ class ParityRun:
         assert normalize(so) == normalize(sg), "schedulers disagree"
         self._mirror_swaps(so)
         if so["status"] != 0:
-            self.runner.apply_swaps(sg)
+            self._gpu_no_batch(sg)
             self.step_idx += 1
             return so["status"], None, None, None
         T = so["num_tokens"]
@@ -147,9 +197,10 @@ class ParityRun:
                                for i in rows]) if rows else np.zeros(0, dtype=np.int64)
         for i in rows:
             self._snapshot(so["block_tables"][i])
-        ds = self.runner.upload(sg)
         gpu_outs, ref_outs = [], []
         bs = sc.block_size
+        qkv, oin = [], []
+        sel = torch.as_tensor(toks, dtype=torch.long, device=self.device)
         for layer in range(sc.num_layers):
             seeds = [workloads.step_seed(sc.seed, self.step_idx, layer, w) for w in range(3)]
             q = workloads.token_tensors(T, sc.num_q_heads, sc.head_dim, seed=seeds[0], dtype=sc.dtype,
@@ -158,13 +209,17 @@ class ParityRun:
                                         scale=sc.value_scale, device=self.device)
             v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[2], dtype=sc.dtype,
                                         scale=sc.value_scale, device=self.device)
+            qkv.append((q, k, v))
             # oracle inputs (copies of the generator's output, before any kernel runs)
-            sel = torch.as_tensor(toks, dtype=torch.long, device=self.device)
-            qo = q.index_select(0, sel).double().cpu().numpy()
-            ko = k.index_select(0, sel).double().cpu().numpy()
-            vo = v.index_select(0, sel).double().cpu().numpy()
-            out = self.runner.run(ds, q, k, v, layer=layer)
-            gpu_outs.append(out.index_select(0, sel).double().cpu().numpy())
+            oin.append((q.index_select(0, sel).double().cpu().numpy(),
+                        k.index_select(0, sel).double().cpu().numpy(),
+                        v.index_select(0, sel).double().cpu().numpy()))
+        outs = self._gpu_step(sg, qkv)
+        for layer in range(sc.num_layers):
+            qo, ko, vo = oin[layer]
+            if check:
+                o = outs[layer]
+                gpu_outs.append(o.index_select(0, sel.to(o.device)).double().cpu().numpy())
             # oracle: append followed rows' tokens into the sub-pool, then attend
             slots = []
             for t in toks:
@@ -172,6 +227,8 @@ class ParityRun:
                 slots.append(self.idx[s // bs] * bs + s % bs)
             paged_kv.append(self.sub_k[layer], self.sub_v[layer], ko, vo,
                             np.asarray(slots, dtype=np.int64), bs)
+            if not check:
+                continue
             cu = [0]
             for i in rows:
                 cu.append(cu[-1] + int(so["cu_seqlens_q"][i + 1] - so["cu_seqlens_q"][i]))
@@ -185,10 +242,14 @@ class ParityRun:
                                        window=sc.sliding_window)
             ref_outs.append(ref)
         assert self.o.step_done() == self.c.step_done()
+        if self.kind == "pipelined":
+            self.runner.synchronize()
         errs = self.runner.workspace.read_errors()
         assert errs == 0, f"device error bits {errs:#x}"
         if self.runner.swap is not None:
             errs = self.runner.swap.read_errors()
             assert errs == 0, f"swap error bits {errs:#x}"
         self.step_idx += 1
+        if not check:
+            return 0, None, None, toks
         return 0, gpu_outs, ref_outs, toks

@@ -259,6 +259,34 @@ def test_full_long_prompt_late_step_sampled():
     _check(g[0], r[0], "bf16", "long prompt step 6")
 
 
+def test_full_long_prompt_late_chunks():
+    """The long-prompt interleave through its whole 32,768-token prompt: 64
+    steps of 512-token chunks at offsets 0 .. 32,256 next to 128 growing
+    decodes (64 Q / 8 KV heads).  The oracle follows decode row 0 and the
+    prompt; every query of chunks 16, 32 and 63 (keys up to 8,704, 16,896
+    and 32,768) is compared element by element."""
+    sc = workloads.long_prompt_32k()
+    run = ParityRun(sc, sample=[0, 128])
+    checks = {16, 32, 63}
+    for step in range(64):
+        st, g, r, toks = run.step(check=step in checks)
+        assert st == 0
+        if step in checks:
+            assert len(toks) == 513
+            _check(g[0], r[0], "bf16", f"long prompt chunk {step}")
+    assert int(run.last["seq_lens"][-1]) == 32768
+
+
+def test_full_prefill_chunk_16k():
+    """The 512-token chunk at offset 16,384 (64 Q / 8 KV heads) that the
+    prefill kernel's counters are quoted on, every query and head."""
+    sc = workloads.prefill_chunk_16k()
+    run = ParityRun(sc)
+    st, g, r, toks = run.step()
+    assert st == 0 and len(toks) == 512
+    _check(g[0], r[0], "bf16", "prefill_chunk_16k")
+
+
 def test_trace_first_steps_sampled_all_layers():
     """The request trace (Poisson arrivals, lognormal lengths, 4 layers with
     their own pools): its first 10 steps with arrivals added per step; the

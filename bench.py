@@ -44,10 +44,36 @@ import workloads  # noqa: E402
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the
-# decode kernel per workload (as ncu prints them: mixed 2048-token step 1.72
-# GB read + 10.32 MB written; 64-request decode step 566.31 MB + 8.71 MB);
-# cleared whenever the kernel changes.
-DECODE_TRAFFIC_BYTES = {"mixed_2048": 1716275968 + 10705152, "decode_64": 566323456 + 8658432}
+# decode kernel per workload, with the digest of the decode kernel's sources
+# the capture was taken on (DECODE_SOURCES); the bench reports the figure
+# only while the sources still have that digest, else null.
+DECODE_SOURCES = ["decode_attention.cuh", "decode_launch.cuh", "decode_launch.h", "decode_bf16.cu",
+                  "device_utils.cuh"]
+DECODE_TRAFFIC = {
+    # 1,716,296,192 B read + 7,247,872 B written (algorithmic 1,714,053,120 B)
+    "mixed_2048": {"bytes": 1716296192 + 7247872, "sha16": "8a9ac9477a96314d"},
+    # 566,316,288 B read + 5,668,352 B written (algorithmic 564,916,224 B)
+    "decode_64": {"bytes": 566316288 + 5668352, "sha16": "8a9ac9477a96314d"},
+}
+
+
+def decode_sources_sha16():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "paged_attention_continuous_gb300", "csrc")
+    for name in DECODE_SOURCES:
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def decode_traffic(workload):
+    """(bytes, digest) of the last capture for this workload if it was taken
+    on the current decode sources, else (None, digest of the capture)."""
+    rec = DECODE_TRAFFIC.get(workload)
+    if rec is None:
+        return None, None
+    return (rec["bytes"] if rec["sha16"] == decode_sources_sha16() else None), rec["sha16"]
 
 
 def peaks():
@@ -320,6 +346,7 @@ def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
     out = torch.empty_like(q)
     tot = {"tokens": 0, "t_step": 0.0, "t_pre": 0.0, "t_dec": 0.0, "flops": 0, "bytes": 0}
     per_step = []
+    worst = None     # (step, TFLOP/s) of the slowest prefill chunk
     steps = 0
     while steps < 64:
         st = sched.schedule_step()
@@ -344,6 +371,10 @@ def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
         by = decode_bytes(st, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, 2)
         tot["tokens"] += T; tot["t_step"] += t_step; tot["t_pre"] += t_pre
         tot["t_dec"] += t_dec; tot["flops"] += fl; tot["bytes"] += by
+        if t_pre:
+            tf = fl / t_pre / 1e12
+            if worst is None or tf < worst[1]:
+                worst = (steps, tf)
         if steps in (0, 16, 32, 48, 63):
             per_step.append({"step": steps, "chunk_start": int(st["seq_lens"][-1]) - int(
                 np.diff(st["cu_seqlens_q"])[-1]), "prefill_tflops": round(fl / t_pre / 1e12, 1) if t_pre else 0,
@@ -363,7 +394,9 @@ def measure_long_prompt(cb, torch, dev, reps, hbm, bf16, bf16s):
                         "peak_tflops": bf16, "frac": round(pt / bf16, 4),
                         "frac_sustained": round(pt / bf16s, 4),
                         "algorithmic_flops": int(tot["flops"]),
-                        "ms_total": round(tot["t_pre"] * 1e3, 3)},
+                        "ms_total": round(tot["t_pre"] * 1e3, 3),
+                        "slowest_chunk": {"step": worst[0], "tflops": round(worst[1], 1),
+                                          "frac": round(worst[1] / bf16, 4)} if worst else None},
             "decode": {"kernel": "decode_kernel", "achieved_gbs": round(dg, 1), "peak_gbs": hbm,
                        "frac": round(dg / hbm, 4)},
             "sampled_steps": per_step, "reps_per_step": reps}
@@ -672,11 +705,112 @@ def choose_oracle_rows(step, budget_rows):
     return sorted(set(int(x) for x in dec)), pre
 
 
+def config_dict(sc, step, world):
+    """The workload description both arms report (same keys and values)."""
+    elem = 2 if sc.dtype == "bf16" else 4
+    dbytes = decode_bytes(step, sc.num_q_heads, sc.num_kv_heads, sc.head_dim, elem)
+    return {"workload": sc.name, "num_tokens": int(step["num_tokens"]),
+            "num_reqs": int(step["num_reqs"]), "num_decodes": int(step["num_decodes"]),
+            "q_heads": sc.num_q_heads, "kv_heads": sc.num_kv_heads,
+            "head_dim": sc.head_dim, "block_size": sc.block_size,
+            "num_blocks": sc.num_blocks, "max_batch_tokens": sc.max_batch_tokens,
+            "l2": "inputs larger than L2 (decode KV %.2f GB per step), no flush" % (dbytes / 1e9),
+            "parallelism": f"replicas x{world}"}
+
+
+def measure_e2e(cb, torch, dev, sc, runner, rank, world, args):
+    """The step end to end through the public C API with host buffers: one
+    cb_executor_run_step per step -- the C scheduler call, pinned host ->
+    device copies of the step's metadata and q/k/v, cb_kv_append +
+    cb_paged_attention, and the device -> host copy of the output --
+    double-buffered over copy-in / compute / copy-out streams.  The
+    scheduler advances from the workload's first step.  The running
+    requests are the workload's (long decodes and the in-flight prefill);
+    its waiting prompts, and new prompts of the same length distribution
+    (U[64, 1024] tokens) arriving so that four always wait, get 1-4 output
+    tokens, so requests finish, the row cap never binds, and every step
+    stays a budget-filled mix of about a hundred decodes and prefill chunks
+    like the first.  Also reports the device-only rate of the same steps
+    (the executor's CUDA events around each step's kernels)."""
+    K = max(1, args.e2e_steps)
+    rng = np.random.default_rng(4242 + rank)
+    sched = cb.Scheduler(block_size=sc.block_size, num_blocks=sc.num_blocks,
+                         max_batch_tokens=sc.max_batch_tokens,
+                         max_requests_per_batch=sc.max_requests_per_batch,
+                         max_blocks_per_seq=sc.max_blocks_per_seq,
+                         max_prefill_chunk=sc.max_prefill_chunk, safety_margin=sc.safety_margin,
+                         free_list=sc.free_list)
+    for r in sc.running:
+        sched.add_running_request(r.req_id, r.prompt_len, r.output_len, r.num_cached)
+    for w in sc.waiting:
+        sched.add_request(w.req_id, w.prompt_len, int(rng.integers(1, 5)))
+    Tm = sc.max_batch_tokens
+    ex = cb.Executor(runner.k_cache, runner.v_cache, num_q_heads=sc.num_q_heads,
+                     max_reqs=sc.max_requests_per_batch, max_tokens=Tm,
+                     max_blocks_per_seq=sc.max_blocks_per_seq, scale=sc.softmax_scale)
+    mk = lambda h, seed: workloads.token_tensors(Tm, h, sc.head_dim, seed=seed, dtype=sc.dtype,
+                                                  scale=sc.value_scale, device="cpu").pin_memory()
+    hq, hk, hv = mk(sc.num_q_heads, 901), mk(sc.num_kv_heads, 902), mk(sc.num_kv_heads, 903)
+    ho = torch.empty((Tm, sc.num_q_heads, sc.head_dim), dtype=hq.dtype, pin_memory=True)
+    next_id = [10 ** 7]
+
+    def top_up():
+        waiting = sched.counts()[1]
+        while waiting < 4:
+            sched.add_request(next_id[0], int(rng.integers(64, 1025)), int(rng.integers(1, 5)))
+            next_id[0] += 1
+            waiting += 1
+
+    for _ in range(3):
+        top_up()
+        ex.run_step(sched, hq, hk, hv, ho)
+    ex.synchronize()
+    ex.reset_stats()
+    elem = hq.element_size()
+    W = sc.max_blocks_per_seq
+    h2d = d2h = 0
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        top_up()
+        T, R = ex.run_step(sched, hq, hk, hv, ho)
+        h2d += 4 * ((R + 1) + R + R * W + T) + T * (sc.num_q_heads + 2 * sc.num_kv_heads) * \
+            sc.head_dim * elem
+        d2h += T * sc.num_q_heads * sc.head_dim * elem
+    ex.synchronize()
+    t = time.perf_counter() - t0
+    steps, toks, cms = ex.stats()
+    assert ex.read_errors() == 0
+    ex.close()
+    tok_all, t_all, dev_s = float(toks), t, cms / 1e3
+    if world > 1:
+        dist = torch.distributed
+        t_all = reduce_over_ranks(dist, t, dist.ReduceOp.MAX, dev)
+        dev_s = reduce_over_ranks(dist, dev_s, dist.ReduceOp.MAX, dev)
+        tok_all = reduce_over_ranks(dist, toks, dist.ReduceOp.SUM, dev)
+    value = tok_all / t_all
+    dev_value = tok_all / dev_s if dev_s else 0.0
+    return {"value": round(value, 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d / K), "d2h_bytes_per_step": int(d2h / K),
+            "steps": int(steps), "tokens": int(toks),
+            "device_value": round(dev_value, 1),
+            "frac_of_device": round(value / dev_value, 4) if dev_value else None,
+            "includes": "per step: cb_executor_run_step = cb_schedule_step + pinned H2D of the "
+                        "step's metadata and q/k/v + cb_kv_append + cb_paged_attention + D2H of "
+                        "the output + cb_step_done, double-buffered (copy-in / compute / "
+                        "copy-out streams); the scheduler advances from the workload's first "
+                        "step (prompts get 1-4 output tokens, arrivals keep four waiting, "
+                        "steps stay budget-filled); timed from the first "
+                        "call to the last output on the host; device_value = the same steps' "
+                        "tokens / the sum of their kernel times (CUDA events)"}
+
+
 # ----------------------------------------------------------------- main
 def run_ours(args, rank, world):
     import torch
     import paged_attention_continuous_gb300 as cb
-    from paged_attention_continuous_gb300.step import PipelinedStepRunner
+    from paged_attention_continuous_gb300.step import StepRunner
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -687,8 +821,8 @@ def run_ours(args, rank, world):
     assert step["status"] == 0
     T, R, nd = step["num_tokens"], step["num_reqs"], step["num_decodes"]
     # the kernel timings below use upload/run on the current stream; the
-    # end-to-end loop uses the same runner's pipelined submit afterwards
-    runner = PipelinedStepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
+    # end-to-end loop runs the C step executor on the same caches afterwards
+    runner = StepRunner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
                                  num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim,
                                  dtype=sc.dtype, max_reqs=sc.max_requests_per_batch,
                                  max_tokens=sc.max_batch_tokens,
@@ -766,34 +900,10 @@ def run_ours(args, rank, world):
         dist.barrier()
     assert ws.read_errors() == 0
 
-    # ---- end to end through the public API, host buffers
-    e2e_steps = min(K, args.e2e_steps)
-    scheds = [load_c_scheduler(cb, sc) for _ in range(e2e_steps + 1)]
-    hq = q.cpu().pin_memory(); hk = k.cpu().pin_memory(); hv = v.cpu().pin_memory()
-    houts = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
-    meta_bytes = 4 * ((R + 1) + R + R * sc.max_blocks_per_seq + T)
+    # ---- end to end through the public API: the C step executor
+    e2e = measure_e2e(cb, torch, dev, sc, runner, rank, world, args)
 
-    def e2e_step(s, i):
-        # host scheduling of this step overlaps the device's previous step;
-        # the step's inputs go in and its output comes back on copy streams
-        st = s.schedule_step()
-        return runner.submit(st, hq, hk, hv, houts[i % 2])
-
-    torch.cuda.synchronize()
-    e2e_step(scheds[-1], 0)  # warm
-    runner.synchronize()
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_step(scheds[i], i)
-    runner.synchronize()
-    t_e2e = time.perf_counter() - t0
-    h2d_meta = meta_bytes
-    if world > 1:
-        dist = torch.distributed
-        t_e2e = reduce_over_ranks(dist, t_e2e, dist.ReduceOp.MAX, dev)
-    h2d = h2d_meta + (hq.numel() + hk.numel() + hv.numel()) * hq.element_size()
-    d2h = houts[0].numel() * houts[0].element_size()
-
+    traffic, traffic_sha = decode_traffic(sc.name)
     pk, src = peaks()
     hbm = float(pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bf16 = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -822,25 +932,13 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": sc.dtype,
         "data": "synthetic (seeded N(0,1)*0.5 q/k/v, random-filled KV pool, permuted blocks)",
-        "config": {"workload": sc.name, "num_tokens": T, "num_reqs": R, "num_decodes": nd,
-                   "q_heads": sc.num_q_heads, "kv_heads": sc.num_kv_heads,
-                   "head_dim": sc.head_dim, "block_size": sc.block_size,
-                   "num_blocks": sc.num_blocks, "max_batch_tokens": sc.max_batch_tokens,
-                   "l2": "inputs larger than L2 (decode KV %.2f GB per step), no flush" % (dbytes / 1e9),
-                   "parallelism": f"replicas x{world}"},
-        "e2e": {"value": round(tokens_all * e2e_steps / t_e2e, 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "steps": e2e_steps,
-                "includes": "cb_schedule_step + pinned H2D of metadata and q/k/v + "
-                            "cb_kv_append + cb_paged_attention + D2H of output, every step; "
-                            "PipelinedStepRunner.submit overlaps a step's copies with its "
-                            "neighbours' compute (two buffer sets, copy-in / compute / "
-                            "copy-out streams), timed from the first submit to the last "
-                            "output's arrival on the host"},
+        "config": config_dict(sc, step, world),
+        "e2e": e2e,
         "roofline": {"kernel": "decode_kernel (split-KV, bf16)", "bound": "hbm",
                      "achieved": round(dec_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(dec_gbs / hbm, 4), "peak_source": src,
-                     "traffic": DECODE_TRAFFIC_BYTES.get(sc.name),
+                     "traffic": traffic, "traffic_capture_sha16": traffic_sha,
+                     "kernel_sha16": decode_sources_sha16(),
                      "algorithmic_bytes_per_launch": dbytes,
                      "ms_per_launch": round(dec_s * 1e3, 4)},
         "prefill": {"kernel": "prefill rows", "bound": "tensor",
@@ -869,6 +967,21 @@ def run_ours(args, rank, world):
             "trace": measure_trace(cb, torch, dev, hbm, bf16, sc=workloads.sliding_trace(0),
                                    desc="sliding_trace (32 requests, window 384, 512-block "
                                         "pool, 2 layers, 32Q/8KV)")}
+    # compact copies of the fractions the targets are judged on
+    fr = {"mixed_2048_decode_hbm": line["roofline"]["frac"],
+          "mixed_2048_prefill_tensor": line["prefill"]["frac"]}
+    if "decode_only" in line:
+        fr["decode_64_hbm"] = line["decode_only"]["frac"]
+        lp = line["long_prompt"]
+        fr["long_prompt_decode_hbm"] = lp["decode"]["frac"]
+        fr["long_prompt_prefill_tensor"] = lp["prefill"]["frac"]
+        if lp["prefill"].get("slowest_chunk"):
+            fr["long_prompt_slowest_chunk_tensor"] = lp["prefill"]["slowest_chunk"]["frac"]
+        fr["window_decode_hbm"] = line["sliding_window"]["decode"]["frac"]
+    fr["e2e_frac_of_device"] = line["e2e"].get("frac_of_device")
+    items = list(line.items())
+    k_at = [k for k, _ in items].index("prefill") + 1
+    line = dict(items[:k_at] + [("fractions", fr)] + items[k_at:])
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sc, step, runner, q, k, v, torch, dev,
                                             budget_s=args.cpu_seconds)
@@ -970,11 +1083,12 @@ def run_reference(args, rank, world):
                                 scale=sc.value_scale, device=dev)
     v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[2], dtype=sc.dtype,
                                 scale=sc.value_scale, device=dev)
+    # each step: one pass of the oracle over every row of the step (the rows
+    # the cpu_baseline leg times)
     total = args.steps + args.warmup
-    budget = max(0.2, min(20.0, 150.0 / max(total, 1)))
     tot_tok, tot_s = 0, 0.0
     for i in range(total):
-        cb = cpu_baseline(sc, step, None, q, k, v, torch, dev, budget_s=budget, full=False)
+        cb = cpu_baseline(sc, step, None, q, k, v, torch, dev, budget_s=0.0, full=True)
         if i >= args.warmup:
             tot_tok += cb["value"] * cb["seconds"]
             tot_s += cb["seconds"]
@@ -983,7 +1097,7 @@ def run_reference(args, rank, world):
             "value": round(val, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(tot_s / max(args.steps, 1) * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic", "config": {"workload": sc.name},
+            "dtype": "f64", "data": "synthetic", "config": config_dict(sc, step, world),
             "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"],
                              "value": round(val, 2)},
             "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -998,7 +1112,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixed_2048",
                     choices=["mixed_2048", "decode_64", "long_prompt_32k", "prefill_chunk_16k"])
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",

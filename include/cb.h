@@ -489,6 +489,86 @@ cb_status cb_debug_inject_wait_timeout(uint64_t wait_ns, int32_t decode_item,
                                        int32_t prefill_tile);
 
 /* ------------------------------------------------------------------------
+ * Step executor (host + GPU).  "Continuous batching architecture", Async
+ * batching: the host schedules step N+1 while the device computes step N,
+ * and step N+1's inputs and step N-1's output cross the CPU-GPU link at the
+ * same time.  An executor owns two sets of device buffers (q, k_new, v_new,
+ * out for every layer, and the packed step metadata), a pinned staging
+ * buffer per set, a workspace, and three streams (copy-in, compute,
+ * copy-out); the KV caches stay the caller's.  Steps use the two sets in
+ * turn.  For one step, cb_executor_submit packs the step's host metadata
+ * into the set's pinned buffer and queues: the metadata and every layer's
+ * q/k/v rows host -> device (after the set's previous compute); per layer
+ * cb_kv_append + cb_paged_attention (after that copy and after the set's
+ * previous copy-out); every layer's output rows device -> host.  It returns
+ * without waiting.
+ *
+ *   config        caches: device [num_blocks][Hkv][block_size][D] per layer
+ *                 (host arrays of num_layers pointers, copied); sizes bound
+ *                 every later step (max_reqs rows, max_tokens tokens,
+ *                 block tables of max_blocks_per_seq columns).
+ *   q/k/v_host    host [num_layers] pointers to [T][H][D] rows of the step
+ *                 (pinned memory keeps the copies asynchronous; other host
+ *                 memory is copied synchronously); they must stay unchanged
+ *                 until cb_executor_synchronize.
+ *   out_host      host [num_layers] pointers receiving [T][Hq][D]; complete
+ *                 after cb_executor_synchronize.
+ * Steps that carry offload swaps are refused (CB_ERR_UNSUPPORTED): the
+ * executor does not own a swap pool.  create allocates device and pinned
+ * memory; submit and run_step allocate nothing.
+ * ---------------------------------------------------------------------- */
+typedef struct cb_executor cb_executor;
+
+typedef struct cb_executor_config {
+  int32_t num_layers;
+  void* const* k_caches;        /* host [num_layers] device pointers */
+  void* const* v_caches;
+  int32_t num_blocks;
+  int32_t block_size;           /* 16 */
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  cb_dtype dtype;
+  float scale;                  /* softmax scale */
+  int32_t sliding_window;       /* 0: full attention */
+  int32_t max_reqs;
+  int32_t max_tokens;
+  int32_t max_blocks_per_seq;
+} cb_executor_config;
+
+cb_status cb_executor_create(const cb_executor_config* cfg, cb_executor** out);
+void cb_executor_destroy(cb_executor* ex);
+
+/* Queue one scheduled step (see above); an empty step is a no-op. */
+cb_status cb_executor_submit(cb_executor* ex, const cb_step* step,
+                             const void* const* q_host, const void* const* k_host,
+                             const void* const* v_host, void* const* out_host);
+
+/* Schedule the next step of `sched`, submit it, and commit it with
+ * cb_step_done: one call per serving step.  *num_tokens / *num_reqs get the
+ * step's token and row counts (0 for an empty step; either may be NULL).
+ * Returns cb_schedule_step's status when that is not CB_OK (the step is
+ * then neither submitted nor committed). */
+cb_status cb_executor_run_step(cb_executor* ex, cb_sched* sched,
+                               const void* const* q_host, const void* const* k_host,
+                               const void* const* v_host, void* const* out_host,
+                               int32_t* num_tokens, int32_t* num_reqs);
+
+/* Wait until every queued copy and kernel has finished. */
+cb_status cb_executor_synchronize(cb_executor* ex);
+
+/* Steps and tokens submitted, and the compute stream's time spent on them
+ * (CUDA events around each step's kernels; steps still running are not
+ * counted yet).  Any output pointer may be NULL. */
+cb_status cb_executor_stats(cb_executor* ex, int64_t* steps, int64_t* tokens,
+                            double* compute_ms);
+cb_status cb_executor_reset_stats(cb_executor* ex);
+
+/* Synchronize, then read and clear the device error bits of the executor's
+ * appends and attention calls; CB_ERR_DEVICE_CHECK if any was set. */
+cb_status cb_executor_read_errors(cb_executor* ex, uint32_t* bits);
+
+/* ------------------------------------------------------------------------
  * cb_paged_decode_noalloc (GPU).  No counterpart in the pages: an extra
  * entry point for callers that cannot allocate device memory.
  *

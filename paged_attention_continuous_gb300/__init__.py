@@ -101,6 +101,16 @@ class cb_attention_args(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t), ("sliding_window", ctypes.c_int32)]
 
 
+class cb_executor_config(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("k_caches", ctypes.POINTER(ctypes.c_void_p)),
+                ("v_caches", ctypes.POINTER(ctypes.c_void_p)), ("num_blocks", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("sliding_window", ctypes.c_int32), ("max_reqs", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32)]
+
+
 SWAP_MAX_POOLS = 128
 
 
@@ -143,6 +153,16 @@ def _declare():
     L.cb_paged_attention.argtypes = [P(cb_attention_args), vp]
     L.cb_attention_read_errors.argtypes = [vp, sz, vp, P(ctypes.c_uint32)]
     L.cb_debug_inject_wait_timeout.argtypes = [ctypes.c_uint64, i32, i32]
+    PV = P(vp)
+    L.cb_executor_create.argtypes = [P(cb_executor_config), P(vp)]
+    L.cb_executor_destroy.argtypes = [vp]
+    L.cb_executor_destroy.restype = None
+    L.cb_executor_submit.argtypes = [vp, P(cb_step), PV, PV, PV, PV]
+    L.cb_executor_run_step.argtypes = [vp, vp, PV, PV, PV, PV, P(i32), P(i32)]
+    L.cb_executor_synchronize.argtypes = [vp]
+    L.cb_executor_stats.argtypes = [vp, P(i64), P(i64), P(ctypes.c_double)]
+    L.cb_executor_reset_stats.argtypes = [vp]
+    L.cb_executor_read_errors.argtypes = [vp, P(ctypes.c_uint32)]
     for name in ("cb_sched_create", "cb_add_request", "cb_add_request_tokens",
                  "cb_sched_prefix_stats", "cb_sched_hold_blocks", "cb_sched_release_blocks",
                  "cb_add_running_request",
@@ -151,7 +171,9 @@ def _declare():
                  "cb_validate_step",
                  "cb_attention_workspace_init",
                  "cb_paged_attention", "cb_attention_read_errors",
-                 "cb_debug_inject_wait_timeout"):
+                 "cb_debug_inject_wait_timeout", "cb_executor_create", "cb_executor_submit",
+                 "cb_executor_run_step", "cb_executor_synchronize", "cb_executor_stats",
+                 "cb_executor_reset_stats", "cb_executor_read_errors"):
         getattr(L, name).restype = ctypes.c_int
 
 
@@ -475,6 +497,108 @@ def inject_wait_timeout(wait_ns: int = 0, decode_item: int = -1, prefill_tile: i
     _check(_lib.cb_debug_inject_wait_timeout(int(wait_ns), int(decode_item), int(prefill_tile)))
 
 
+def _ptrs(ts):
+    ts = list(ts) if isinstance(ts, (list, tuple)) else [ts]
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts]), ts
+
+
+class Executor:
+    """cb_executor: a whole serving step behind one C call, double-buffered
+    over copy-in / compute / copy-out streams.  ``k_caches``/``v_caches``:
+    per layer device tensors [num_blocks, Hkv, 16, D] (the caller keeps
+    them).  ``run_step(sched, q, k, v, out)`` schedules the next step of a
+    ``Scheduler``, queues its copies and kernels and commits it; q/k/v/out
+    are per layer pinned host tensors with at least the step's T rows (one
+    tensor for a single layer).  Results are in ``out`` after
+    ``synchronize()``."""
+
+    def __init__(self, k_caches, v_caches, *, num_q_heads: int, max_reqs: int, max_tokens: int,
+                 max_blocks_per_seq: int, scale: float, sliding_window: int = 0):
+        kc = list(k_caches) if isinstance(k_caches, (list, tuple)) else [k_caches]
+        vc = list(v_caches) if isinstance(v_caches, (list, tuple)) else [v_caches]
+        _need_cuda(*kc, *vc)
+        nb, hkv, bs, d = kc[0].shape
+        self._kp = (ctypes.c_void_p * len(kc))(*[t.data_ptr() for t in kc])
+        self._vp = (ctypes.c_void_p * len(vc))(*[t.data_ptr() for t in vc])
+        self._caches = (kc, vc)
+        cfg = cb_executor_config(len(kc), ctypes.cast(self._kp, ctypes.POINTER(ctypes.c_void_p)),
+                                 ctypes.cast(self._vp, ctypes.POINTER(ctypes.c_void_p)), nb, bs,
+                                 num_q_heads, hkv, d, _dtype_code(kc[0]), float(scale),
+                                 int(sliding_window), max_reqs, max_tokens, max_blocks_per_seq)
+        h = ctypes.c_void_p()
+        _check(_lib.cb_executor_create(ctypes.byref(cfg), ctypes.byref(h)))
+        self._h = h
+        self.num_layers = len(kc)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.cb_executor_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def _bufs(self, q, k, v, out):
+        (qp, qs), (kp, ks), (vp, vs), (op, os_) = _ptrs(q), _ptrs(k), _ptrs(v), _ptrs(out)
+        if not (len(qs) == len(ks) == len(vs) == len(os_) == self.num_layers):
+            raise ValueError("one q/k/v/out tensor per layer expected")
+        for t in qs + ks + vs + os_:
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError("executor inputs and outputs are contiguous host tensors")
+        P = ctypes.POINTER(ctypes.c_void_p)
+        return [ctypes.cast(x, P) for x in (qp, kp, vp, op)]
+
+    def run_step(self, sched, q, k, v, out):
+        """One serving step of ``sched`` (schedule + submit + commit); returns
+        (tokens, rows) of the step.  Raises CBError(CB_ERR_NO_BLOCKS) when
+        nothing could be scheduled."""
+        bufs = self._bufs(q, k, v, out)
+        n, r = ctypes.c_int32(), ctypes.c_int32()
+        _check(_lib.cb_executor_run_step(self._h, sched._h, *bufs, ctypes.byref(n), ctypes.byref(r)))
+        return int(n.value), int(r.value)
+
+    def submit(self, step: dict, q, k, v, out) -> None:
+        """Queue a step already scheduled (the dict ``Scheduler.schedule_step``
+        returns); its arrays are packed before this returns."""
+        bufs = self._bufs(q, k, v, out)
+        R, T = int(step["num_reqs"]), int(step["num_tokens"])
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        arrs = [np.ascontiguousarray(step[k_], dtype=np.int32)
+                for k_ in ("cu_seqlens_q", "seq_lens", "block_tables", "slot_mapping")]
+        bt = arrs[2].reshape(R, -1) if R else arrs[2].reshape(0, 1)
+        c = cb_step()
+        c.num_reqs, c.num_tokens, c.num_decodes = R, T, int(step["num_decodes"])
+        c.max_q_len = int(step.get("max_q_len", 1))
+        c.max_seq_len = int(step.get("max_seq_len", 1))
+        c.max_blocks_per_seq = int(bt.shape[1])
+        c.cu_seqlens_q = arrs[0].ctypes.data_as(i32p)
+        c.seq_lens = arrs[1].ctypes.data_as(i32p)
+        c.block_tables = arrs[2].ctypes.data_as(i32p)
+        c.slot_mapping = arrs[3].ctypes.data_as(i32p)
+        c.num_swap_in = len(step.get("swap_in", ()))
+        c.num_swap_out = len(step.get("swap_out", ()))
+        _check(_lib.cb_executor_submit(self._h, ctypes.byref(c), *bufs))
+
+    def synchronize(self) -> None:
+        _check(_lib.cb_executor_synchronize(self._h))
+
+    def stats(self):
+        """(steps, tokens, compute milliseconds) since creation or reset."""
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_double()
+        _check(_lib.cb_executor_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+        return int(a.value), int(b.value), float(c.value)
+
+    def reset_stats(self) -> None:
+        _check(_lib.cb_executor_reset_stats(self._h))
+
+    def read_errors(self) -> int:
+        bits = ctypes.c_uint32()
+        st = _lib.cb_executor_read_errors(self._h, ctypes.byref(bits))
+        if st not in (CB_OK, CB_ERR_DEVICE_CHECK):
+            _check(st)
+        return int(bits.value)
+
+
 def paged_attention_args(**kw) -> cb_attention_args:
     """Build a raw cb_attention_args (for callers that drive the C ABI
     directly, e.g. with CUDA graphs)."""
@@ -482,4 +606,5 @@ def paged_attention_args(**kw) -> cb_attention_args:
 
 
 __all__ = ["Scheduler", "kv_append", "kv_swap", "validate_step", "paged_attention", "Workspace", "workspace_size",
+           "Executor",
            "CBError", "version", "library", "LIB_PATH"]

@@ -26,7 +26,7 @@ ROOT = os.path.dirname(HERE)
 
 SOURCES = ["scheduler.cpp", "kv_append.cu", "attention.cu", "prefill_attention.cu",
            "decode_bf16.cu", "decode_f32.cu", "decode_noalloc.cu", "kv_swap.cu", "validate.cpp",
-           "tensor_map.cpp", "launch_common.cpp"]
+           "tensor_map.cpp", "launch_common.cpp", "executor.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-lineinfo",
           "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

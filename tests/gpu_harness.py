@@ -32,7 +32,7 @@ def tolerance_ok(gpu: np.ndarray, ref: np.ndarray, dtype: str):
     return bool((err <= bound).all()), float(err.max(initial=0.0)), float((err - bound).max(initial=-1))
 
 
-RUNNERS = ("eager", "graph", "pipelined")
+RUNNERS = ("eager", "graph", "pipelined", "native", "native_run")
 
 
 class ParityRun:
@@ -43,7 +43,10 @@ class ParityRun:
     (StepRunner: upload + append + attention on the current stream),
     "graph" (GraphStepRunner: the step padded to its bucket and replayed
     from a CUDA graph) or "pipelined" (PipelinedStepRunner: inputs and
-    output in pinned host memory, copied on their own streams)."""
+    output in pinned host memory, copied on their own streams), "native"
+    (the C step executor, cb_executor_submit, on the C scheduler's step) or
+    "native_run" (cb_executor_run_step: the executor itself schedules,
+    submits and commits each step of the C scheduler)."""
 
     def __init__(self, sc, sample=None, device="cuda", fill_seed=1234, max_tokens=None,
                  arrivals=False, runner="eager"):
@@ -65,8 +68,8 @@ class ParityRun:
         else:
             load_scenario(self.o, sc)
             load_scenario(self.c, sc)
-        Runner = {"eager": StepRunner, "graph": GraphStepRunner,
-                  "pipelined": PipelinedStepRunner}[runner]
+        Runner = {"eager": StepRunner, "graph": GraphStepRunner, "pipelined": PipelinedStepRunner,
+                  "native": StepRunner, "native_run": StepRunner}[runner]
         self.runner = Runner(num_blocks=sc.num_blocks, num_q_heads=sc.num_q_heads,
                                  num_kv_heads=sc.num_kv_heads, head_dim=sc.head_dim,
                                  dtype=sc.dtype, max_reqs=sc.max_requests_per_batch,
@@ -76,6 +79,14 @@ class ParityRun:
                                  swap_blocks=sc.swap_blocks, sliding_window=sc.sliding_window)
         self.device = device
         self.torch = torch
+        self.ex = None
+        if runner.startswith("native"):
+            import paged_attention_continuous_gb300 as cb
+            self.ex = cb.Executor(self.runner.k_cache, self.runner.v_cache,
+                                  num_q_heads=sc.num_q_heads, max_reqs=sc.max_requests_per_batch,
+                                  max_tokens=max_tokens or sc.max_batch_tokens,
+                                  max_blocks_per_seq=self.c_width(),
+                                  scale=self.runner.scale, sliding_window=sc.sliding_window)
         self.pristine = []
         for layer in range(sc.num_layers):
             kp = workloads.cache_fill(sc.num_blocks, sc.num_kv_heads, sc.block_size, sc.head_dim,
@@ -98,6 +109,10 @@ class ParityRun:
         self.oswap = {}
         self.swap_pairs = 0
         self.step_idx = 0
+
+    def c_width(self):
+        """Block-table width of the C scheduler's steps."""
+        return int(self.runner.W)
 
     def _followed(self, rid):
         return self.sample is None or int(rid) in self.sample
@@ -152,11 +167,20 @@ class ParityRun:
                 r.v_buf[layer][:T].copy_(v)
             r.run(key)
             return [r.out_buf[layer][:T] for layer in range(len(qkv))]
-        # pipelined: the step's inputs and output live in pinned host memory
+        # the host paths: the step's inputs and output live in pinned host memory
         hq = [q.cpu().pin_memory() for q, _, _ in qkv]
         hk = [k.cpu().pin_memory() for _, k, _ in qkv]
         hv = [v.cpu().pin_memory() for _, _, v in qkv]
         ho = [self.torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for q, _, _ in qkv]
+        if self.kind == "native":
+            self.ex.submit(sg, hq, hk, hv, ho)
+            self.ex.synchronize()
+            return ho
+        if self.kind == "native_run":
+            n, _ = self.ex.run_step(self.c, hq, hk, hv, ho)
+            assert n == T, (n, T)
+            self.ex.synchronize()
+            return ho
         r.submit(sg, hq, hk, hv, ho).synchronize()
         return ho
 
@@ -166,6 +190,9 @@ class ParityRun:
         if self.kind == "pipelined":
             with self.torch.cuda.stream(self.runner.compute_stream):
                 self.runner.apply_swaps(sg)
+            return
+        if self.kind == "native_run":
+            assert self.c.schedule_step()["status"] == sg["status"]
             return
         self.runner.apply_swaps(sg)
 
@@ -183,9 +210,12 @@ class ParityRun:
                 add_waiting(self.c, w)
                 self.next_arrival += 1
         so = self.o.schedule_step()
-        sg = self.c.schedule_step()
+        if self.kind == "native_run":
+            sg = so     # the executor schedules the C scheduler's step itself
+        else:
+            sg = self.c.schedule_step()
+            assert normalize(so) == normalize(sg), "schedulers disagree"
         self.last = so
-        assert normalize(so) == normalize(sg), "schedulers disagree"
         self._mirror_swaps(so)
         if so["status"] != 0:
             self._gpu_no_batch(sg)
@@ -241,10 +271,13 @@ class ParityRun:
                                        so["seq_lens"][rows], bt, bs, sc.softmax_scale,
                                        window=sc.sliding_window)
             ref_outs.append(ref)
-        assert self.o.step_done() == self.c.step_done()
+        if self.kind == "native_run":
+            self.o.step_done()      # the executor committed the C scheduler's step
+        else:
+            assert self.o.step_done() == self.c.step_done()
         if self.kind == "pipelined":
             self.runner.synchronize()
-        errs = self.runner.workspace.read_errors()
+        errs = self.ex.read_errors() if self.ex is not None else self.runner.workspace.read_errors()
         assert errs == 0, f"device error bits {errs:#x}"
         if self.runner.swap is not None:
             errs = self.runner.swap.read_errors()

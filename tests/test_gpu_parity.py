@@ -287,6 +287,24 @@ def test_full_prefill_chunk_16k():
     _check(g[0], r[0], "bf16", "prefill_chunk_16k")
 
 
+def test_prefill_short_chunks_long_context():
+    """Short chunks of long requests: few query tiles, each against
+    hundreds of KV tiles -- two requests with 192- and 64-token chunks at
+    offsets 30,000 and 12,000 (64 Q / 8 KV heads), every query compared."""
+    running = [workloads.RunningRequest(0, 30192, 4, 30000),
+               workloads.RunningRequest(1, 12064, 4, 12000)]
+    nb = 3000
+    sc = workloads.Scenario(
+        name="short_chunks", num_q_heads=64, num_kv_heads=8, head_dim=128, dtype="bf16",
+        num_blocks=nb, max_batch_tokens=256, max_requests_per_batch=4, max_prefill_chunk=0,
+        safety_margin=0.0, max_blocks_per_seq=0, free_list=workloads.permuted_free_list(nb, 9),
+        running=running, waiting=[], value_scale=0.5)
+    run = ParityRun(sc)
+    st, g, r, toks = run.step()
+    assert st == 0 and len(toks) == 256
+    _check(g[0], r[0], "bf16", "short chunks, long context")
+
+
 def test_trace_first_steps_sampled_all_layers():
     """The request trace (Poisson arrivals, lognormal lengths, 4 layers with
     their own pools): its first 10 steps with arrivals added per step; the

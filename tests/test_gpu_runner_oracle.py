@@ -1,13 +1,16 @@
-"""The CUDA-graph and pipelined step paths against the oracle, directly.
+"""The CUDA-graph, pipelined and native-executor step paths against the
+oracle, directly.
 
 "Continuous batching architecture" (CUDA graphs; Async batching): the graph
 runner pads each step to a power-of-two bucket and replays a captured graph
 (padding rows of query length 0 and seq_len 0, padding tokens of slot -1,
-which the eager path never sends), and the pipelined runner takes its
-inputs and returns its output in pinned host memory, copied on their own
-streams.  Each is run step by step next to the oracle (its own scheduler,
-append and attention) on the same seeded inputs, and compared element by
-element at the bf16 bound: |gpu - oracle| <= 2e-2 + 1e-2 |oracle|.
+which the eager path never sends); the pipelined runner and the C step
+executor (cb_executor_submit, and cb_executor_run_step, which also
+schedules and commits each step itself) take their inputs and return their
+output in pinned host memory, copied on their own streams.  Each is run step
+by step next to the oracle (its own scheduler, append and attention) on the
+same seeded inputs, and compared element by element at the bf16 bound:
+|gpu - oracle| <= 2e-2 + 1e-2 |oracle|.
 """
 import pytest
 
@@ -17,7 +20,8 @@ from tests.test_gpu_parity import _mixed_small
 
 pytestmark = pytest.mark.gpu
 
-RUNNERS = ["graph", "pipelined"]
+RUNNERS = ["graph", "pipelined", "native", "native_run"]
+SWAP_RUNNERS = ["graph", "pipelined"]   # the executor owns no swap pool
 
 
 def _check_all(run, g, r, what):
@@ -54,7 +58,7 @@ def test_runner_trace_steps_match_oracle(runner):
     assert seen > 0
 
 
-@pytest.mark.parametrize("runner", RUNNERS)
+@pytest.mark.parametrize("runner", SWAP_RUNNERS)
 def test_runner_offload_trace_matches_oracle(runner):
     """The whole memory-pressure trace (swaps and soft resets) until every
     request has finished."""

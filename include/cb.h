@@ -596,8 +596,11 @@ cb_status cb_executor_read_errors(cb_executor* ex, uint32_t* bits);
  * (more room lets it cut the caches into more, smaller splits); larger
  * calls are rejected with CB_ERR_INVALID_ARG and a message giving the sizes.
  * Set-up: the first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.
+ * (cudaGetSymbolAddress) with that device current.  With CUDA's default
+ * lazy module loading, the library's module -- and with it the 64 MiB
+ * array -- is put on a device when the module is first needed there, at
+ * the latest by that first call: a caller that cannot allocate later makes
+ * the first call at set-up time, and before any stream capture.
  * Every call clears the counters it needs, then uses the array;
  * all calls in the process share it, so calls that may overlap on the GPU
  * (different streams without ordering between them) race with each other.

@@ -186,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* B = reinterpret_cast<Bars*>(smem + SmemLayout::bars);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // the producers' tensor maps travel to the TMA unit while the rows are scanned
+  if ((warp == 8 || warp == 9) && lane == 0) tc::prefetch_tensormap(warp == 8 ? &p.tmap_k : &p.tmap_v);
 
   const int G = p.group;
   const int tpt = kBM / G;                       // tokens per query tile
@@ -266,6 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int j_lo = key_lo / kBN;
   const int lo_pg = key_lo / kPage;
   const int nt = n_tiles - j_lo;
+  // Lane pg (0..7) of a producer warp looks up the block of page pg of a KV
+  // tile; the first tile's ids are requested here, so the lookups overlap
+  // the barrier and tensor-memory set-up below.
+  auto page_in = [&](int j) {
+    const int page = j * (kBN / kPage) + lane;
+    return lane < kBN / kPage && j < n_tiles && page < npages && page >= lo_pg;
+  };
+  auto page_blk = [&](int j) {
+    return __ldg(p.block_tables + (int64_t)r * W + j * (kBN / kPage) + lane);
+  };
+  bool in0 = false;
+  int blk0 = 0;
+  if (warp == 8 || warp == 9) {
+    in0 = page_in(j_lo);
+    if (in0) blk0 = page_blk(j_lo);
+  }
 
   if (threadIdx.x == 0) {
     // a stage is free once every active MMA issuer (one per query tile)
@@ -300,21 +318,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= 8 && warp < kMmaWarp) {
     // ------------------------------------------------------------ producers
-    // Warp 8 streams K tiles, warp 9 V tiles.  Lane pg (0..7) looks up the
-    // block of page pg of a tile (the next tile's ids are requested while the
-    // current tile waits for a free stage); lane 0 issues the two boxes of
-    // every page.  A page outside the sequence or the table uses a row past
-    // the end of the tensor map, which the TMA engine reads as zeros.
+    // Warp 8 streams K tiles, warp 9 V tiles.  Lane pg (0..7) holds the
+    // block of page pg of a tile (the next tile's ids are requested before
+    // the current tile's copies are issued, and read only afterwards); lane
+    // 0 issues the two boxes of every page.  A page outside the sequence or
+    // the table uses a row past the end of the tensor map, which the TMA
+    // engine reads as zeros.
     const int hv = warp - 8;  // 0: K, 1: V
     const CUtensorMap* tmap = hv ? &p.tmap_v : &p.tmap_k;
     const int nst = hv ? kStagesV : kStagesK;
     const uint32_t ring = hv ? SmemLayout::v : SmemLayout::k;
     const int oob_row = p.num_blocks * p.num_kv_heads * kPage;
-    auto page_row = [&](int j) -> int {
-      const int page = j * (kBN / kPage) + lane;
+    // tensor-map row of a looked-up page
+    auto page_row = [&](bool in, int blk) -> int {
       int row = oob_row;
-      if (lane < kBN / kPage && j < n_tiles && page < npages && page >= lo_pg) {
-        const int blk = __ldg(p.block_tables + (int64_t)r * W + page);
+      if (in) {
         if (blk >= 0 && blk < p.num_blocks)
           row = (blk * p.num_kv_heads + g) * kPage;
         else if (hv == 0)
@@ -322,11 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return row;
     };
-    int row_next = page_row(j_lo);
+    bool in_next = in0;
+    int blk_next = blk0;
     int issued = 0;
     for (int jj = 0; jj < nt; ++jj) {
-      const int row = row_next;
-      row_next = page_row(j_lo + jj + 1);  // in flight while we wait
+      const int row = page_row(in_next, blk_next);
+      in_next = page_in(j_lo + jj + 1);    // in flight while this tile is issued
+      if (in_next) blk_next = page_blk(j_lo + jj + 1);
       const int s = jj % nst;
       uint64_t* full = hv ? &B->v_full[s] : &B->k_full[s];
       if (jj >= nst) {

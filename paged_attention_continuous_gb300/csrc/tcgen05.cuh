@@ -112,6 +112,12 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ---- TMA: 2-D tiled load global -> shared, completion on an mbarrier -------
+// Fetch a tensor map (a kernel parameter or global memory) into the TMA
+// unit's descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32_t y,
                                             uint64_t* bar) {
   asm volatile(

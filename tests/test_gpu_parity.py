@@ -84,8 +84,10 @@ EDGE_CTX = [2, 3, 15, 16, 17, 31, 32, 33, 100, 255, 256, 257, 1000, 2049]
 
 
 @pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64), ("f32", 128), ("bf16", 64)])
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (32, 8), (16, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (32, 8), (16, 2), (64, 4)])
 def test_decode_edges(dtype, D, Hq, Hkv):
+    """GQA 1, 2, 4, 8 and 16 (bf16: the matrix-instruction instantiations,
+    seven warps per CTA at 16; fp32 at 16: the CUDA-core fallback)."""
     sc = _decode_scenario(EDGE_CTX, Hq, Hkv, D, dtype)
     run = ParityRun(sc)
     st, g, r, _ = run.step()
@@ -105,7 +107,7 @@ def test_decode_many_splits_and_rows():
 
 
 @pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 32, 8, 128), ("bf16", 64, 8, 128),
-                                            ("f32", 16, 4, 128)])
+                                            ("bf16", 64, 4, 128), ("f32", 16, 4, 128)])
 def test_decode_few_long_rows(dtype, Hq, Hkv, D):
     """A handful of very long caches next to tiny ones: each long row is cut
     into hundreds of splits (both phases), merged in the same kernel by the

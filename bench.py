@@ -50,10 +50,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 DECODE_SOURCES = ["decode_attention.cuh", "decode_launch.cuh", "decode_launch.h", "decode_bf16.cu",
                   "device_utils.cuh"]
 DECODE_TRAFFIC = {
-    # 1,716,296,192 B read + 7,247,872 B written (algorithmic 1,714,053,120 B)
-    "mixed_2048": {"bytes": 1716296192 + 7247872, "sha16": "8a9ac9477a96314d"},
-    # 566,316,288 B read + 5,668,352 B written (algorithmic 564,916,224 B)
-    "decode_64": {"bytes": 566316288 + 5668352, "sha16": "8a9ac9477a96314d"},
+    # 1,716,280,320 B read + 6,918,400 B written (algorithmic 1,714,053,120 B)
+    "mixed_2048": {"bytes": 1716280320 + 6918400, "sha16": "cdf8addc958ddc46"},
+    # 566,309,888 B read + 5,074,176 B written (algorithmic 564,916,224 B)
+    "decode_64": {"bytes": 566309888 + 5074176, "sha16": "cdf8addc958ddc46"},
 }
 
 

@@ -12,12 +12,12 @@
 //   * Work item = (decode row r, split s, KV head g): a run of consecutive
 //     16-token pages of one request and one KV head.  The items come in two
 //     phases: first the leading 7/8 of every row's pages in equal large
-//     splits, dealt out statically (warp w of W takes items w, w + W, ...),
-//     then the remaining 1/8 in small splits handed out in index order
-//     through a global atomic counter, so the last items are short and the
-//     warps finish together.  Split sizes are chosen in the kernel from the
-//     total page count, and doubled until the splits fit the caller's
-//     partial slots.
+//     splits, about one per warp, then the remaining 1/8 in small splits.
+//     Warp w of W starts with item w; every later item is drawn in index
+//     order from a global atomic counter (large items first), so the last
+//     items are short and the warps finish together.  Split sizes are chosen
+//     in the kernel from the total page count, and doubled until the splits
+//     fit the caller's partial slots.
 //   * Every WARP is an independent worker with its own pipeline: lane 0 issues
 //     the copies of the (block, head) K page and V page into a ring of
 //     kStages shared-memory stages, each tracked by an mbarrier; the ring
@@ -514,12 +514,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const __grid_con
 
   // Look-ahead: the item after the producer's current one is decoded, and
   // its first block ids requested, one item early, so that the block-table
-  // load does not stall an item change.  Phase-A items come from the static
-  // deal (next_static); phase-B indices from the counter, whose next value
-  // lane 0 keeps in flight.
+  // load does not stall an item change.  Indices after a warp's first come
+  // from the counter, whose next value lane 0 keeps in flight.
   const int items_a = num_a * Hkv;
   const uint32_t worker = blockIdx.x * kWarps + warp;
-  int next_static = (int)worker;
+  // a warp's first item is dealt statically (item w); every later one is
+  // drawn from the counter in index order, phase A's large items first
+  const uint32_t n_static = (uint32_t)min((int64_t)items_a, (int64_t)total_workers);
+  bool first_static = worker < n_static;
   uint32_t pref_idx = 0;
   lane0_fetch_add1(p.work_counter, pref_idx, lane);
   // idx / Hkv without a division: floor(idx * ceil(2^32 / Hkv) / 2^32) is
@@ -551,18 +553,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const __grid_con
   auto fetch_ahead = [&]() {
     nx_ok = false;
     uint32_t idx;
-    if (next_static < items_a) {
-      idx = (uint32_t)next_static;
-      next_static += (int)total_workers;
+    if (first_static) {
+      idx = worker;
+      first_static = false;
     } else {
       const uint32_t b = __shfl_sync(0xffffffffu, pref_idx, 0);
-      const uint32_t items_b = (uint32_t)(total_items - items_a);
-      if (b >= items_b) {
-        if (b == items_b + total_workers - 1 && lane == 0) atomicExch(p.work_counter, 0u);
+      const uint32_t items_dyn = (uint32_t)total_items - n_static;
+      if (b >= items_dyn) {
+        if (b == items_dyn + total_workers - 1 && lane == 0) atomicExch(p.work_counter, 0u);
         return;
       }
       lane0_fetch_add1(p.work_counter, pref_idx, lane);
-      idx = (uint32_t)items_a + b;
+      idx = n_static + b;
     }
     const uint32_t u = (uint32_t)(((uint64_t)idx * hkv_magic) >> 32);
     const int g = (int)(idx - u * (uint32_t)Hkv);

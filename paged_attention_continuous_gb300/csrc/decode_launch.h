@@ -12,7 +12,7 @@
 namespace cb {
 namespace decode {
 
-constexpr int kItemsA = 2;          // phase-A items per warp (target)
+constexpr int kItemsA = 1;          // phase-A items per warp (target)
 constexpr int kItemsB = 1;          // phase-B items per warp (target)
 constexpr int kPlanMax = 1024;      // decode rows planned per launch
 // Partial slots a call should provide for `rows` decode rows: kSlotsPerRow

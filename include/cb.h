@@ -346,8 +346,9 @@ cb_status cb_validate_step(const int32_t* cu_seqlens_q, const int32_t* seq_lens,
  *   k_cache, v_cache device [num_blocks][Hkv][block_size][D] (dtype)
  *   error_word    optional device uint32; a slot >= num_blocks*block_size is
  *                 skipped and sets CB_DEVERR_SLOT_RANGE there.
- * D * sizeof(dtype) must be a multiple of 16 bytes and every pointer 16-byte
- * aligned.  Bit-exact copy.
+ * D * sizeof(dtype) must be 16 bytes times a power of two (every head size
+ * the attention takes) and every pointer 16-byte aligned; at most 2^31
+ * 16-byte vectors per call (CB_ERR_UNSUPPORTED otherwise).  Bit-exact copy.
  * ---------------------------------------------------------------------- */
 cb_status cb_kv_append(const void* k_new, const void* v_new,
                        const int32_t* slot_mapping, int32_t num_tokens,
@@ -437,6 +438,17 @@ typedef struct cb_attention_args {
                                    p-W+1..p only, and table entries of pages
                                    wholly before a row's window are never
                                    read (they may be -1); 0: full attention */
+  int32_t after_append;         /* 1: the kernel queued just before on the
+                                   stream is the cb_kv_append of this step
+                                   (the append of "vLLM serving internals",
+                                   PagedAttention as a virtual memory system);
+                                   the decode kernel then starts while the
+                                   append finishes (programmatic dependent
+                                   launch), plans its work meanwhile and reads
+                                   the cache only once the append is complete.
+                                   0: plain stream order.  Setting it when the
+                                   kernel before is not that append is
+                                   undefined. */
 } cb_attention_args;
 
 /* Device error bits (cb_attention_read_errors / cb_kv_append error_word). */

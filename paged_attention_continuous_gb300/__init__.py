@@ -98,7 +98,8 @@ class cb_attention_args(ctypes.Structure):
                 ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("dtype", ctypes.c_int32), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("sliding_window", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_size_t), ("sliding_window", ctypes.c_int32),
+                ("after_append", ctypes.c_int32)]
 
 
 class cb_executor_config(ctypes.Structure):
@@ -468,10 +469,13 @@ class Workspace:
 
 def paged_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens, block_tables, *,
                     num_decodes: int, max_q_len: int, max_seq_len: int, scale: float,
-                    workspace: Workspace, out=None, stream=None, sliding_window: int = 0):
+                    workspace: Workspace, out=None, stream=None, sliding_window: int = 0,
+                    after_append: bool = False):
     """cb_paged_attention.  q [T, Hq, D]; caches [num_blocks, Hkv, bs, D];
     metadata int32 device tensors; ``sliding_window`` > 0 for a
-    sliding-window layer.  Returns out [T, Hq, D]."""
+    sliding-window layer; ``after_append``: the launch just before on the
+    stream was this step's kv_append (the decode kernel then overlaps its
+    end).  Returns out [T, Hq, D]."""
     torch = _torch()
     _need_cuda(q, k_cache, v_cache, cu_seqlens_q, seq_lens, block_tables)
     if out is None:
@@ -485,7 +489,7 @@ def paged_attention(q, k_cache, v_cache, cu_seqlens_q, seq_lens, block_tables, *
                           cu_seqlens_q.data_ptr(), seq_lens.data_ptr(), block_tables.data_ptr(),
                           R, num_decodes, T, max_q_len, max_seq_len, nb, block_tables.shape[1],
                           bs, hq, hkv, d, float(scale), _dtype_code(q), workspace.ptr,
-                          workspace.nbytes, int(sliding_window))
+                          workspace.nbytes, int(sliding_window), int(bool(after_append)))
     _check(_lib.cb_paged_attention(ctypes.byref(a), _stream_ptr(stream)))
     return out
 

@@ -366,10 +366,6 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const __grid_con
   __shared__ int32_t s_red2[kWarps];
   __shared__ int32_t s_spa, s_spb;
 
-  // a kernel launched after this one with programmatic serialization (the
-  // prefill rows of the same call, which read nothing this kernel writes)
-  // may start on SMs this grid has left
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nthreads = kWarps * 32;
@@ -719,6 +715,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const __grid_con
     }
   };
 
+  // The cache is read from here on.  Launched right after the step's K/V
+  // append (programmatic dependent launch), the grid planned while the
+  // append finished and waits for it here (a no-op otherwise).  Only then
+  // may a kernel launched after this one with programmatic serialization
+  // (the prefill rows of the same call, which read nothing this kernel
+  // writes but do read the appended K/V) start on the SMs this grid leaves.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int s = 0; s < kStages; ++s) produce(s);
 
   if constexpr (kMma) {

@@ -71,8 +71,21 @@ cb_status launch(const cb_attention_args& a, const Scratch& s, uint32_t* error_w
   for (int r0 = 0; r0 < a.num_decodes; r0 += kPlanMax) {
     p.row_begin = r0;
     p.num_rows = a.num_decodes - r0 < kPlanMax ? a.num_decodes - r0 : kPlanMax;
-    kern<<<grid, kWarps * 32, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    // the first launch may overlap the step's K/V append queued just before
+    // (the kernel waits for it before reading the cache); later launches
+    // share this call's workspace with the one before and follow it fully
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute lattr[1];
+    lattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    lattr[0].val.programmaticStreamSerializationAllowed = (r0 == 0 && a.after_append) ? 1 : 0;
+    cfg.attrs = lattr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return fail(CB_ERR_CUDA, "decode kernel launch: %s", cudaGetErrorString(e));
   }
   return CB_OK;

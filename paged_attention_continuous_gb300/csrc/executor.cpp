@@ -268,6 +268,7 @@ extern "C" cb_status cb_executor_submit(cb_executor* ex, const cb_step* step,
   a.workspace = ex->ws;
   a.workspace_bytes = ex->ws_bytes;
   a.sliding_window = c.sliding_window;
+  a.after_append = 1;  // each layer's attention follows its append on comp_s
   for (int l = 0; l < c.num_layers; ++l) {
     cb_status st = cb_kv_append(s.k[l], s.v[l], s.meta_dev + o3, T, ex->k_caches[l], ex->v_caches[l],
                                 c.num_blocks, c.num_kv_heads, c.head_dim, c.block_size, c.dtype,

@@ -9,7 +9,8 @@
 // Layout: new rows [T][Hkv][D]; cache [num_blocks][Hkv][block_size][D].  Each
 // thread moves one 16-byte vector of K and the matching one of V: loads are
 // fully coalesced over (t, h, vector), and each (t, h) row lands as
-// D*elem contiguous bytes in the cache.
+// D*elem contiguous bytes in the cache.  The row loads are issued before the
+// slot lookup they do not depend on.
 #include <cuda_runtime.h>
 
 #include "cb_error.h"
@@ -21,28 +22,34 @@ namespace cb {
 __global__ void __launch_bounds__(256) kv_append_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int32_t* __restrict__ slot_mapping, int32_t num_tokens, uint4* __restrict__ k_cache,
-    uint4* __restrict__ v_cache, int64_t num_slots, int32_t num_kv_heads, int32_t vecs_per_row,
+    uint4* __restrict__ v_cache, int64_t num_slots, int32_t num_kv_heads, int32_t vec_shift,
     int32_t block_shift, int32_t block_mask, uint32_t* error_word) {
-  const int64_t per_token = (int64_t)num_kv_heads * vecs_per_row;
-  const int64_t total = (int64_t)num_tokens * per_token;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int32_t t = (int32_t)(i / per_token);
-    const int32_t rem = (int32_t)(i - (int64_t)t * per_token);  // h * vecs + c
+  // the attention launch that follows (when it asks for it) may start now;
+  // it reads the cache only after this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // 32-bit indices (the host checks that they fit): thread i moves vector c
+  // of row (t, h) = i >> vec_shift
+  const int32_t total = (num_tokens * num_kv_heads) << vec_shift;
+  const int32_t vec_mask = (1 << vec_shift) - 1;
+  for (int32_t i = (int32_t)(blockIdx.x * blockDim.x + threadIdx.x); i < total;
+       i += (int32_t)(gridDim.x * blockDim.x)) {
+    const int32_t row = i >> vec_shift;
+    const int32_t c = i & vec_mask;
+    const int32_t t = row / num_kv_heads;
+    const int32_t h = row - t * num_kv_heads;
+    const uint4 kv = __ldg(k_new + i);
+    const uint4 vv = __ldg(v_new + i);
     const int32_t slot = __ldg(slot_mapping + t);
     if (slot < 0) continue;
     if ((int64_t)slot >= num_slots) {
       set_error(error_word, CB_DEVERR_SLOT_RANGE);
       continue;
     }
-    const int32_t h = rem / vecs_per_row;
-    const int32_t c = rem - h * vecs_per_row;
     const int64_t block = slot >> block_shift;
     const int32_t off = slot & block_mask;
-    const int64_t dst =
-        (((block * num_kv_heads + h) << block_shift) + off) * (int64_t)vecs_per_row + c;
-    k_cache[dst] = __ldg(k_new + i);
-    v_cache[dst] = __ldg(v_new + i);
+    const int64_t dst = ((((block * num_kv_heads + h) << block_shift) + off) << vec_shift) + c;
+    k_cache[dst] = kv;
+    v_cache[dst] = vv;
   }
 }
 
@@ -66,6 +73,11 @@ extern "C" cb_status cb_kv_append(const void* k_new, const void* v_new,
   const int row_bytes = head_dim * elem;
   if (row_bytes % 16 != 0)
     return cb::fail(CB_ERR_UNSUPPORTED, "cb_kv_append: head_dim*elem must be a multiple of 16");
+  const int vecs = row_bytes / 16;
+  if ((vecs & (vecs - 1)) != 0)
+    return cb::fail(CB_ERR_UNSUPPORTED, "cb_kv_append: head_dim*elem/16 must be a power of two");
+  if ((int64_t)num_tokens * num_kv_heads * vecs >= ((int64_t)1 << 31))
+    return cb::fail(CB_ERR_UNSUPPORTED, "cb_kv_append: more than 2^31 16-byte vectors in one call");
   const uintptr_t align = (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_cache | (uintptr_t)v_cache;
   if (align & 15u) return cb::fail(CB_ERR_INVALID_ARG, "cb_kv_append: pointers must be 16-byte aligned");
   if (cb::validate_enabled()) {
@@ -75,14 +87,15 @@ extern "C" cb_status cb_kv_append(const void* k_new, const void* v_new,
   }
   int shift = 0;
   while ((1 << shift) < block_size) ++shift;
-  const int vecs = row_bytes / 16;
+  int vshift = 0;
+  while ((1 << vshift) < vecs) ++vshift;
   const int64_t total = (int64_t)num_tokens * num_kv_heads * vecs;
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 152 * 64) blocks = 152 * 64;
   cb::kv_append_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(
       (const uint4*)k_new, (const uint4*)v_new, slot_mapping, num_tokens, (uint4*)k_cache,
-      (uint4*)v_cache, (int64_t)num_blocks * block_size, num_kv_heads, vecs, shift,
+      (uint4*)v_cache, (int64_t)num_blocks * block_size, num_kv_heads, vshift, shift,
       block_size - 1, error_word);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cb::fail(CB_ERR_CUDA, "cb_kv_append launch: %s", cudaGetErrorString(e));

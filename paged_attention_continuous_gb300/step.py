@@ -207,7 +207,7 @@ class StepRunner:
                                num_decodes=ds.num_decodes, max_q_len=ds.max_q_len,
                                max_seq_len=ds.max_seq_len, scale=self.scale,
                                workspace=self.workspace, out=out,
-                               sliding_window=self.sliding_window)
+                               sliding_window=self.sliding_window, after_append=True)
 
 
 class PipelinedStepRunner(StepRunner):

@@ -54,6 +54,8 @@ def test_argument_errors_without_gpu():
     assert st == cb.CB_ERR_INVALID_ARG
     st = lib.cb_kv_append(16, 16, 16, 4, 16, 16, 10, 8, 128, 12, 1, None, None)
     assert st == cb.CB_ERR_UNSUPPORTED            # block size not a power of two
+    st = lib.cb_kv_append(16, 16, 16, 4, 16, 16, 10, 8, 96, 16, 1, None, None)
+    assert st == cb.CB_ERR_UNSUPPORTED            # 12 vectors of 16 bytes per row
     a = cb.cb_attention_args()
     a.num_reqs, a.num_tokens, a.num_decodes = 2, 3, 3
     assert lib.cb_paged_attention(ctypes.byref(a), None) == cb.CB_ERR_INVALID_ARG

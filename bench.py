@@ -1000,17 +1000,10 @@ def _pristine_blocks(sc, blocks, dev, torch):
     return k, v
 
 
-def cpu_baseline(sc, step, runner, q, k, v, torch, dev, budget_s=20.0, full=True):
-    """The oracle, as it stands, timed on the host cores on the step's rows:
-    all decode rows and all prefill rows, repeated until about ``budget_s``
-    seconds have passed (``full``); or, when a whole pass would not fit the
-    budget, a spread of decode rows plus each prefill row's last queries."""
-    if full:
-        dec_rows, pre_rows = list(range(step["num_decodes"])), list(range(step["num_decodes"],
-                                                                          step["num_reqs"]))
-    else:
-        dec_rows, pre_rows = choose_oracle_rows(step, 16)
-    rows = dec_rows + pre_rows
+def oracle_setup(sc, step, rows, q, k, v, torch, dev):
+    """The oracle's inputs for ``rows`` of ``step``: the pristine contents of
+    the rows' cache blocks (a compact pool, tables remapped into it) and the
+    step's q/k/v on the host."""
     blocks = sorted({int(b) for r in rows for b in step["block_tables"][r] if b >= 0})
     kpool, vpool = _pristine_blocks(sc, blocks, dev, torch)
     remap = {b: i for i, b in enumerate(blocks)}
@@ -1025,6 +1018,29 @@ def cpu_baseline(sc, step, runner, q, k, v, torch, dev, budget_s=20.0, full=True
                                      int(s) % sc.block_size if (int(s) // sc.block_size) in remap
                                      else -1 for s in step["slot_mapping"]], dtype=np.int64)
     pools = (kpool, vpool, k.float().cpu().numpy(), v.float().cpu().numpy(), q.float().cpu().numpy())
+    return st, pools
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        return max(p.get("num_threads", 1) for p in threadpoolctl.threadpool_info())
+    except Exception:
+        return os.cpu_count()
+
+
+def cpu_baseline(sc, step, runner, q, k, v, torch, dev, budget_s=20.0, full=True):
+    """The oracle, as it stands, timed on the host cores on the step's rows:
+    all decode rows and all prefill rows, repeated until about ``budget_s``
+    seconds have passed (``full``); or, when a whole pass would not fit the
+    budget, a spread of decode rows plus each prefill row's last queries."""
+    if full:
+        dec_rows, pre_rows = list(range(step["num_decodes"])), list(range(step["num_decodes"],
+                                                                          step["num_reqs"]))
+    else:
+        dec_rows, pre_rows = choose_oracle_rows(step, 16)
+    rows = dec_rows + pre_rows
+    st, pools = oracle_setup(sc, step, rows, q, k, v, torch, dev)
     if full:
         n_tot, t_tot, passes = 0, 0.0, 0
         while passes == 0 or t_tot < budget_s:
@@ -1044,11 +1060,7 @@ def cpu_baseline(sc, step, runner, q, k, v, torch, dev, budget_s=20.0, full=True
         desc = (f"{sc.name} step 0: {len(dec_rows)} of {step['num_decodes']} decode rows "
                 f"+ the last {cap} queries of each of {len(pre_rows)} prefill rows "
                 f"({n_tot} query tokens), numpy float64")
-    try:
-        import threadpoolctl
-        threads = max(p.get("num_threads", 1) for p in threadpoolctl.threadpool_info())
-    except Exception:
-        threads = os.cpu_count()
+    threads = cpu_threads()
     return {"value": round(n_tot / t_tot, 2), "unit": "tokens/s", "cores": int(threads),
             "host_cpus": os.cpu_count(), "kind": "oracle", "seconds": round(t_tot, 2),
             "sample": desc}
@@ -1083,22 +1095,32 @@ def run_reference(args, rank, world):
                                 scale=sc.value_scale, device=dev)
     v = workloads.token_tensors(T, sc.num_kv_heads, sc.head_dim, seed=seeds[2], dtype=sc.dtype,
                                 scale=sc.value_scale, device=dev)
-    # each step: one pass of the oracle over every row of the step (the rows
-    # the cpu_baseline leg times)
+    # The rows the cpu_baseline leg times (all of the step's).  A first,
+    # untimed full pass sizes the per-step sample so that the K + W steps take
+    # about --ref-seconds: the rows are dealt round-robin into n_parts groups
+    # and step i runs group i mod n_parts.
+    nd, R = step["num_decodes"], step["num_reqs"]
+    rows = list(range(R))
+    st, pools = oracle_setup(sc, step, rows, q, k, v, torch, dev)
+    _, t_full = oracle_sample(sc, st, pools, rows)
     total = args.steps + args.warmup
+    n_parts = max(1, min(R, int(np.ceil(t_full * total / max(args.ref_seconds, 1e-3)))))
+    groups = [rows[i::n_parts] for i in range(n_parts)]
     tot_tok, tot_s = 0, 0.0
     for i in range(total):
-        cb = cpu_baseline(sc, step, None, q, k, v, torch, dev, budget_s=0.0, full=True)
+        n, t = oracle_sample(sc, st, pools, groups[i % n_parts])
         if i >= args.warmup:
-            tot_tok += cb["value"] * cb["seconds"]
-            tot_s += cb["seconds"]
+            tot_tok += n
+            tot_s += t
     val = tot_tok / tot_s if tot_s else 0.0
+    sample = (f"{sc.name} step 0: its {nd} decode and {R - nd} prefill rows dealt round-robin into "
+              f"{n_parts} groups, one group per step (a full pass took {t_full:.2f} s), numpy float64")
     return {"impl": "reference", "metric": "attention tokens/s per mixed step",
             "value": round(val, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(tot_s / max(args.steps, 1) * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic", "config": config_dict(sc, step, world),
-            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"],
+            "cpu_baseline": {"kind": "oracle", "cores": int(cpu_threads()), "sample": sample,
                              "value": round(val, 2)},
             "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -1114,6 +1136,8 @@ def main():
                     choices=["mixed_2048", "decode_64", "long_prompt_32k", "prefill_chunk_16k"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="reference arm: about this many seconds of oracle work in all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the decode-only and long-prompt sub-measurements")

@@ -381,6 +381,43 @@ def test_workspace_reused_across_calls_of_different_sizes():
     assert torch.equal(a, b)
 
 
+def test_attention_after_append_overlap_is_bit_identical():
+    """after_append=True lets the decode kernel start while the step's
+    append finishes (it waits for it before reading the cache); the output
+    must be the same bytes as with plain stream order, over several mixed
+    steps on their own pools, with the append re-run right before each."""
+    cb = _cb()
+    sc = _mixed_small("bf16", 32, 8, 128, seed=3)
+    outs = {}
+    for flag in (False, True):
+        run = ParityRun(sc)
+        res = []
+        for step_i in range(3):
+            st = run.c.schedule_step()
+            assert st["status"] == 0
+            ds = run.runner.upload(st)
+            T = st["num_tokens"]
+            q = workloads.token_tensors(T, 32, 128, seed=10 + step_i, dtype="bf16", scale=0.5,
+                                        device="cuda")
+            k = workloads.token_tensors(T, 8, 128, seed=20 + step_i, dtype="bf16", scale=0.5,
+                                        device="cuda")
+            v = workloads.token_tensors(T, 8, 128, seed=30 + step_i, dtype="bf16", scale=0.5,
+                                        device="cuda")
+            kc, vc = run.runner.k_cache[0], run.runner.v_cache[0]
+            cb.kv_append(k, v, ds.slot_mapping, kc, vc)
+            o = cb.paged_attention(q, kc, vc, ds.cu_seqlens_q, ds.seq_lens, ds.block_tables,
+                                   num_decodes=st["num_decodes"], max_q_len=st["max_q_len"],
+                                   max_seq_len=st["max_seq_len"], scale=sc.softmax_scale,
+                                   workspace=run.runner.workspace, after_append=flag)
+            res.append(o.clone())
+            run.c.step_done()
+        torch.cuda.synchronize()
+        assert run.runner.workspace.read_errors() == 0
+        outs[flag] = res
+    for a, b in zip(outs[False], outs[True]):
+        assert torch.equal(a, b)
+
+
 def test_trace_late_steps_sampled_all_layers():
     """The request trace far past its start: every request runs on the GPU
     (4 layers), while the oracle follows two long-lived requests that

@@ -174,27 +174,43 @@ extern "C" cb_status cb_paged_attention(const cb_attention_args* args, cb_stream
   }
   const int nd = a.num_decodes;
   const int G = a.num_q_heads / a.num_kv_heads;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  uint32_t* ew = reinterpret_cast<uint32_t*>(ws + L.header);
+  const bool tc_prefill = nd < a.num_reqs && a.dtype == CB_DTYPE_BF16 && a.head_dim == 128 &&
+                          cb::prefill_supported(G);
+  auto run_decode = [&](cb::decode::After after) -> cb_status {
+    const cb::decode::Scratch ds = cb::decode_scratch(a, L);
+    cb_status s = a.dtype == CB_DTYPE_BF16 ? cb::decode::dispatch_bf16(a, ds, ew, stream, after)
+                                           : cb::decode::dispatch_f32(a, ds, ew, stream, after);
+    if (s == CB_ERR_UNSUPPORTED) {
+      s = a.dtype == CB_DTYPE_BF16 ? cb::dispatch_simt<__nv_bfloat16>(a, L, 0, nd, 0, nd, stream)
+                                   : cb::dispatch_simt<float>(a, L, 0, nd, 0, nd, stream);
+    }
+    return s;
+  };
+  // Order of the two kernels (they share no data).  Normally the decode rows
+  // go first and the prefill grid starts on the SMs the decode kernel frees
+  // as it ends.  When the prefill grid leaves SMs idle for its whole length
+  // (at least 16 fewer CTAs than SMs) and its CTAs are long (the longest row
+  // holds 16k keys or more), the prefill rows go first and the decode
+  // kernel runs beside them on the idle SMs (programmatic dependent launch).
+  if (nd > 0 && tc_prefill && a.max_seq_len >= 16384 &&
+      cb::prefill_ctas(a) + 16 <= cb::sm_count_current_device()) {
+    cb_status st = cb::launch_prefill_bf16(a, ew, ws + L.prefill, stream, false);
+    if (st == CB_OK) return run_decode(cb::decode::After::kPrefill);
+    if (st != CB_ERR_UNSUPPORTED) return st;
+  }
   cb_status st = CB_OK;
   if (nd > 0) {
-    const cb::decode::Scratch ds = cb::decode_scratch(a, L);
-    uint32_t* ew = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.workspace) + L.header);
-    st = a.dtype == CB_DTYPE_BF16 ? cb::decode::dispatch_bf16(a, ds, ew, stream)
-                                  : cb::decode::dispatch_f32(a, ds, ew, stream);
-    if (st == CB_ERR_UNSUPPORTED) {
-      st = a.dtype == CB_DTYPE_BF16
-               ? cb::dispatch_simt<__nv_bfloat16>(a, L, 0, nd, 0, nd, stream)
-               : cb::dispatch_simt<float>(a, L, 0, nd, 0, nd, stream);
-    }
+    st = run_decode(a.after_append ? cb::decode::After::kAppend : cb::decode::After::kStream);
     if (st != CB_OK) return st;
   }
   if (nd < a.num_reqs) {
     // decode rows hold exactly one token each, so prefill tokens start at nd
-    if (a.dtype == CB_DTYPE_BF16 && a.head_dim == 128 && cb::prefill_supported(G)) {
-      uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    if (tc_prefill) {
       // the decode kernel just queued (if any) reads and writes nothing the
       // prefill rows use: let the prefill grid start on the SMs it frees
-      st = cb::launch_prefill_bf16(a, reinterpret_cast<uint32_t*>(ws + L.header),
-                                   ws + L.prefill, stream, nd > 0);
+      st = cb::launch_prefill_bf16(a, ew, ws + L.prefill, stream, nd > 0);
       if (st != CB_ERR_UNSUPPORTED) return st;
     }
     st = a.dtype == CB_DTYPE_BF16

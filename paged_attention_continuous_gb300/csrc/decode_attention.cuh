@@ -100,6 +100,9 @@ struct Params {
   float* part_ml;          // [slots][Hkv][G][2]
   float* part_acc;         // [slots][Hkv][G][D]
   uint64_t wait_ns;        // limit of every bounded wait
+  int32_t pdl_mode;        // After: 1 wait for the grid before (the append)
+                           // before reading the cache; 2 only the grid's
+                           // completion waits for the one before (prefill)
   int32_t withhold_item;   // test hook: the item with this global index
                            // never gets its first page's copies (-1: none)
 };
@@ -410,7 +413,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const __grid_con
     const int64_t units = tot * Hkv;
     const int64_t units_b = units / kTailDiv;
     const int64_t workers = (int64_t)gridDim.x * kWarps;
-    int64_t spa = (units - units_b + workers * kItemsA - 1) / (workers * kItemsA);
+    // beside a prefill grid (pdl_mode 2) the CTAs start at different times
+    // and draw every item from the counter: smaller items keep their finish
+    // together
+    const int64_t items_a = p.pdl_mode == 2 ? kItemsABeside : kItemsA;
+    int64_t spa = (units - units_b + workers * items_a - 1) / (workers * items_a);
     int64_t spb = (units_b + workers * kItemsB - 1) / (workers * kItemsB);
     if (spa < kMinSplitPages) spa = kMinSplitPages;
     if (spb < 1) spb = 1;
@@ -515,8 +522,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const __grid_con
   const int items_a = num_a * Hkv;
   const uint32_t worker = blockIdx.x * kWarps + warp;
   // a warp's first item is dealt statically (item w); every later one is
-  // drawn from the counter in index order, phase A's large items first
-  const uint32_t n_static = (uint32_t)min((int64_t)items_a, (int64_t)total_workers);
+  // drawn from the counter in index order, phase A's large items first.
+  // Beside a prefill grid most CTAs start only as its CTAs end, so there
+  // every item is drawn from the counter: the CTAs that start first take
+  // more.
+  const uint32_t n_static =
+      p.pdl_mode == 2 ? 0u : (uint32_t)min((int64_t)items_a, (int64_t)total_workers);
   bool first_static = worker < n_static;
   uint32_t pref_idx = 0;
   lane0_fetch_add1(p.work_counter, pref_idx, lane);
@@ -717,11 +728,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const __grid_con
 
   // The cache is read from here on.  Launched right after the step's K/V
   // append (programmatic dependent launch), the grid planned while the
-  // append finished and waits for it here (a no-op otherwise).  Only then
-  // may a kernel launched after this one with programmatic serialization
-  // (the prefill rows of the same call, which read nothing this kernel
-  // writes but do read the appended K/V) start on the SMs this grid leaves.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // append finished and waits for it here (a no-op without such a launch;
+  // skipped when the grid before is the prefill rows of the same call, which
+  // write nothing it reads).  Only then may a kernel launched after this one
+  // with programmatic serialization (the prefill rows of the same call,
+  // which read nothing this kernel writes but do read the appended K/V)
+  // start on the SMs this grid leaves.
+  if (p.pdl_mode != 2) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int s = 0; s < kStages; ++s) produce(s);
 
@@ -1202,6 +1215,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) decode_kernel(const __grid_con
       if (n > 1) ticket(i, g, n);
     }
   }
+  // beside the prefill grid before it: this grid completes only after it
+  if (p.pdl_mode == 2 && blockIdx.x == 0 && threadIdx.x == 0)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace decode

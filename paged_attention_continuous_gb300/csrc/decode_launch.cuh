@@ -26,7 +26,7 @@ constexpr int warps_for() {
 
 template <typename T, int D, int G, bool kWindow>
 cb_status launch(const cb_attention_args& a, const Scratch& s, uint32_t* error_word,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, After after) {
   constexpr int kStages = 2;
   constexpr int kWarps = warps_for<T, D, G, kStages>();
   constexpr size_t smem = smem_bytes<T, D, G, kWarps, kStages>();
@@ -71,9 +71,9 @@ cb_status launch(const cb_attention_args& a, const Scratch& s, uint32_t* error_w
   for (int r0 = 0; r0 < a.num_decodes; r0 += kPlanMax) {
     p.row_begin = r0;
     p.num_rows = a.num_decodes - r0 < kPlanMax ? a.num_decodes - r0 : kPlanMax;
-    // the first launch may overlap the step's K/V append queued just before
-    // (the kernel waits for it before reading the cache); later launches
-    // share this call's workspace with the one before and follow it fully
+    // the first launch may overlap the kernel queued just before it (After);
+    // later launches share this call's workspace with the one before and
+    // follow it fully
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
@@ -81,7 +81,9 @@ cb_status launch(const cb_attention_args& a, const Scratch& s, uint32_t* error_w
     cfg.stream = stream;
     cudaLaunchAttribute lattr[1];
     lattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    lattr[0].val.programmaticStreamSerializationAllowed = (r0 == 0 && a.after_append) ? 1 : 0;
+    const After mode = r0 == 0 ? after : After::kStream;
+    p.pdl_mode = (int32_t)mode;
+    lattr[0].val.programmaticStreamSerializationAllowed = mode != After::kStream ? 1 : 0;
     cfg.attrs = lattr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);

@@ -132,8 +132,9 @@ extern "C" cb_status cb_paged_decode_noalloc(const cb_attention_args* args, uint
   ds.part_ml = reinterpret_cast<float*>(scratch + L.part_ml);
   ds.part_acc = reinterpret_cast<float*>(scratch + L.part_acc);
   ds.slots = L.slots;
-  st = a.dtype == CB_DTYPE_BF16 ? cb::decode::dispatch_bf16(a, ds, error_word, stream)
-                                : cb::decode::dispatch_f32(a, ds, error_word, stream);
+  const cb::decode::After after = a.after_append ? cb::decode::After::kAppend : cb::decode::After::kStream;
+  st = a.dtype == CB_DTYPE_BF16 ? cb::decode::dispatch_bf16(a, ds, error_word, stream, after)
+                                : cb::decode::dispatch_f32(a, ds, error_word, stream, after);
   if (st == CB_ERR_UNSUPPORTED)
     return fail(CB_ERR_UNSUPPORTED, "no-alloc decode: head_dim %d with %d query heads per KV head",
                 a.head_dim, G);

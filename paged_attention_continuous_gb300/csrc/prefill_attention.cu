@@ -186,6 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* B = reinterpret_cast<Bars*>(smem + SmemLayout::bars);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // the decode rows of the same call, when launched after this grid with
+  // programmatic serialization, may start at once on the SMs it leaves idle
+  // (they touch nothing this grid touches)
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the producers' tensor maps travel to the TMA unit while the rows are scanned
   if ((warp == 8 || warp == 9) && lane == 0) tc::prefetch_tensormap(warp == 8 ? &p.tmap_k : &p.tmap_v);
 
@@ -610,6 +614,17 @@ bool prefill_supported(int group) {
 
 size_t prefill_workspace_bytes(int64_t, int64_t, int64_t) { return 0; }
 
+int64_t prefill_ctas(const cb_attention_args& a) {
+  using namespace prefill;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  if (G <= 0 || G > kBM) return 0;
+  const int tpp = 2 * (kBM / G);  // tokens per CTA (a pair of query tiles)
+  // every row's pairs: at most (prefill tokens) / tpp rounded up per row
+  const int64_t pairs = ((int64_t)a.num_tokens - a.num_decodes + tpp - 1) / tpp +
+                        (a.num_reqs - a.num_decodes);
+  return pairs > 0 ? pairs * a.num_kv_heads : 0;
+}
+
 cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, uint8_t*,
                               cudaStream_t stream, bool overlap_previous) {
   using namespace prefill;
@@ -647,13 +662,10 @@ cb_status launch_prefill_bf16(const cb_attention_args& a, uint32_t* error_word, 
   p.error_word = error_word;
   p.wait_ns = wait_limit_ns();
   p.withhold_tile = withheld_prefill_tile();
-  const int tpp = 2 * (kBM / G);  // tokens per CTA (a pair of query tiles)
-  // every row's pairs: at most (prefill tokens) / tpp rounded up per row
-  const int64_t pairs = ((int64_t)a.num_tokens - a.num_decodes + tpp - 1) / tpp +
-                        (a.num_reqs - a.num_decodes);
-  if (pairs <= 0) return CB_OK;
-  if (pairs * a.num_kv_heads >= ((int64_t)1 << 31)) return CB_ERR_UNSUPPORTED;
-  dim3 grid((unsigned)(pairs * a.num_kv_heads), 1, 1);
+  const int64_t ctas = prefill_ctas(a);
+  if (ctas <= 0) return CB_OK;
+  if (ctas >= ((int64_t)1 << 31)) return CB_ERR_UNSUPPORTED;
+  dim3 grid((unsigned)ctas, 1, 1);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -17,6 +17,11 @@ bool prefill_supported(int group);
 // that must read zero between calls; independent of the call's sizes).
 size_t prefill_workspace_bytes(int64_t Hq, int64_t Hkv, int64_t D);
 
+// CTAs the prefill-chunk kernel launches for the prefill rows of `a` (an
+// upper bound on the (row, pair of query tiles) units times the KV heads;
+// 0 without prefill rows).
+int64_t prefill_ctas(const cb_attention_args& a);
+
 // Launch the prefill-chunk kernel over rows [num_decodes, num_reqs) (bf16,
 // head_dim 128).  Returns CB_ERR_UNSUPPORTED if it cannot take this call.
 // overlap_previous: the kernel queued just before on `stream` is the decode

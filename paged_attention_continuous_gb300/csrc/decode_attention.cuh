@@ -15,8 +15,10 @@
 //     splits, about one per warp, then the remaining 1/8 in small splits.
 //     Warp w of W starts with item w; every later item is drawn in index
 //     order from a global atomic counter (large items first), so the last
-//     items are short and the warps finish together.  Split sizes are chosen
-//     in the kernel from the total page count, and doubled until the splits
+//     items are short and the warps finish together.  Launched beside a
+//     prefill grid (whose CTAs hold most SMs at first), every item comes
+//     from the counter and phase A is cut finer.  Split sizes are chosen in
+//     the kernel from the total page count, and doubled until the splits
 //     fit the caller's partial slots.
 //   * Every WARP is an independent worker with its own pipeline: lane 0 issues
 //     the copies of the (block, head) K page and V page into a ring of

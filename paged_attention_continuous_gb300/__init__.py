@@ -192,9 +192,20 @@ def library():
 
 # --------------------------------------------------------------- scheduler
 def _arr(ptr, n, dtype):
+    """A numpy copy of n elements of `dtype` (the C element type) at ptr:
+    one memmove into a fresh array (cheaper per call than building a ctypes
+    array view)."""
+    out = np.empty(n, dtype=dtype)
+    if n:
+        ctypes.memmove(out.__array_interface__["data"][0], ptr, n * out.itemsize)
+    return out
+
+
+def _pairs(a_ptr, b_ptr, n):
+    """[n, 2] int32 of two C int32 arrays side by side."""
     if n == 0:
-        return np.zeros(0, dtype=dtype)
-    return np.ctypeslib.as_array(ptr, shape=(n,)).astype(dtype, copy=True)
+        return np.zeros((0, 2), dtype=np.int32)
+    return np.stack([_arr(a_ptr, n, np.int32), _arr(b_ptr, n, np.int32)], axis=1)
 
 
 POLICY_FIFO, POLICY_PREFILL_FIRST = 0, 1
@@ -295,10 +306,8 @@ class Scheduler:
             "slot_mapping": _arr(s.slot_mapping, T, np.int32),
             "stalled_ids": _arr(s.stalled_ids, s.num_stalled, np.int64),
             "stalled_demand": _arr(s.stalled_demand, s.num_stalled, np.int32),
-            "swap_in": np.stack([_arr(s.swap_in_slots, s.num_swap_in, np.int32),
-                                 _arr(s.swap_in_blocks, s.num_swap_in, np.int32)], axis=1),
-            "swap_out": np.stack([_arr(s.swap_out_blocks, s.num_swap_out, np.int32),
-                                  _arr(s.swap_out_slots, s.num_swap_out, np.int32)], axis=1),
+            "swap_in": _pairs(s.swap_in_slots, s.swap_in_blocks, s.num_swap_in),
+            "swap_out": _pairs(s.swap_out_blocks, s.swap_out_slots, s.num_swap_out),
         }
 
     def swapped(self):

@@ -68,3 +68,36 @@ def test_sub_step_slices_rows_and_tokens():
     assert sub["max_q_len"] == 5 and sub["max_seq_len"] == 30
     dec = bench._sub_step(st, 0, 2)
     assert dec["num_decodes"] == 2 and dec["num_tokens"] == 2
+
+
+def test_reference_arm_sizes_its_sample_to_the_budget(monkeypatch):
+    """The reference arm deals the step's rows round-robin into groups so
+    that K + W steps take about --ref-seconds of oracle time, runs group
+    i mod n in step i, and reports the timed steps' query tokens over their
+    oracle seconds, under the same config object as the GPU arm."""
+    import types
+    calls = []
+
+    def fake_setup(sc, step, rows, q, k, v, torch, dev):
+        return step, None
+
+    def fake_sample(sc, st, pools, rows, prefill_token_cap=None):
+        calls.append(list(rows))
+        return len(rows), 0.01 * len(rows)   # 10 ms of oracle time per row
+
+    monkeypatch.setattr(bench, "oracle_setup", fake_setup)
+    monkeypatch.setattr(bench, "oracle_sample", fake_sample)
+    args = types.SimpleNamespace(workload="mixed_2048", steps=20, warmup=3, ref_seconds=2.0)
+    line = bench.run_reference(args, 0, 1)
+    R = line["config"]["num_reqs"]
+    full = calls[0]
+    assert full == list(range(R))                      # the sizing pass: every row
+    n_parts = int(np.ceil(0.01 * R * 23 / 2.0))
+    groups = calls[1:]
+    assert len(groups) == 23
+    assert groups[0] == list(range(0, R, n_parts))
+    assert sorted(r for g in groups[:n_parts] for r in g) == list(range(R))
+    timed = groups[3:]
+    assert line["value"] == pytest.approx(sum(len(g) for g in timed) /
+                                          sum(0.01 * len(g) for g in timed), rel=1e-6)
+    assert bench.run_reference(args, 1, 2) is None     # other ranks do no work
